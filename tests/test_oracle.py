@@ -1,0 +1,217 @@
+"""Pins for the fp64 oracle: each check rests on something other than the oracle itself
+(a closed form, an exact identity, brute force, or the arithmetic printed on the pages).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as M
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rand_case(rng, n_h=3, L=7, scale_w=1.0 / math.sqrt(512)):
+    q = rng.standard_normal((n_h, 192))
+    c = rng.standard_normal((L, 512))
+    kr = rng.standard_normal((L, 64))
+    wk = rng.standard_normal((n_h, 128, 512)) * scale_w
+    wv = rng.standard_normal((n_h, 128, 512)) * scale_w
+    return q, c, kr, wk, wv
+
+
+# ------------------------------- RoPE ---------------------------------------------
+def test_rope_zero_position_is_identity():
+    x = np.random.default_rng(1).standard_normal((5, 64))
+    np.testing.assert_array_equal(M.rope(x, 0), x)
+
+
+def test_rope_preserves_norm():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((9, 64))
+    pos = rng.integers(0, 131072, size=9)
+    y = M.rope(x, pos)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+
+
+def test_rope_closed_form_unit_vectors():
+    # e_0 at position 1 rotates by exactly 1 radian into the (0, 32) plane.
+    e0 = np.zeros(64); e0[0] = 1.0
+    y = M.rope(e0, 1)
+    assert y[0] == pytest.approx(math.cos(1.0), abs=1e-15)
+    assert y[32] == pytest.approx(math.sin(1.0), abs=1e-15)
+    assert np.count_nonzero(np.abs(y) > 1e-15) == 2
+    # e_32 goes the other way: x'_0 = -sin, x'_32 = cos.
+    e32 = np.zeros(64); e32[32] = 1.0
+    y = M.rope(e32, 1)
+    assert y[0] == pytest.approx(-math.sin(1.0), abs=1e-15)
+    assert y[32] == pytest.approx(math.cos(1.0), abs=1e-15)
+    # pair i = 5 turns with frequency 10000^(-10/64).
+    e5 = np.zeros(64); e5[5] = 1.0
+    p = 12345
+    ang = p * 10000.0 ** (-10.0 / 64.0)
+    y = M.rope(e5, p)
+    assert y[5] == pytest.approx(math.cos(ang), abs=1e-12)
+    assert y[37] == pytest.approx(math.sin(ang), abs=1e-12)
+
+
+def test_rope_relative_position_invariance():
+    # Shifting the query and every key position by the same amount leaves the
+    # attention result unchanged (RoPE encodes only relative position).
+    rng = np.random.default_rng(3)
+    q, c, kr_raw, wk, wv = _rand_case(rng, n_h=2, L=6)
+    t = np.arange(6)
+    base = M.attend_explicit(q, c, M.rope(kr_raw, t), wk, wv, pos_q=5)
+    for delta in (1, 1000, 100000):
+        sh = M.attend_explicit(q, c, M.rope(kr_raw, t + delta), wk, wv, pos_q=5 + delta)
+        np.testing.assert_allclose(sh["o"], base["o"], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(sh["lse"], base["lse"], rtol=1e-9)
+
+
+# --------------------------- attention identities ---------------------------------
+def test_absorbed_matches_explicit_bruteforce_sizes():
+    rng = np.random.default_rng(4)
+    for n_h, L in [(1, 1), (2, 3), (4, 8), (3, 5)]:
+        q, c, kr, wk, wv = _rand_case(rng, n_h=n_h, L=L)
+        a = M.attend_explicit(q, c, kr, wk, wv, pos_q=L - 1)
+        b = M.attend_absorbed(q, c, kr, wk, wv, pos_q=L - 1)
+        for k in ("o", "o_lat", "lse"):
+            np.testing.assert_allclose(a[k], b[k], rtol=1e-12, atol=1e-13)
+
+
+def _scalar_loop_attention(q, c, kr, wk, wv, pos_q, scale):
+    """Brute force with Python scalars only (no NumPy linear algebra)."""
+    n_h, L = q.shape[0], c.shape[0]
+    out = []
+    for h in range(n_h):
+        qr = [0.0] * 64
+        for i in range(32):
+            th = pos_q * 10000.0 ** (-2.0 * i / 64.0)
+            qr[i] = q[h, 128 + i] * math.cos(th) - q[h, 160 + i] * math.sin(th)
+            qr[32 + i] = q[h, 160 + i] * math.cos(th) + q[h, 128 + i] * math.sin(th)
+        s = []
+        vs = []
+        for t in range(L):
+            acc = 0.0
+            for d in range(128):
+                k_d = sum(wk[h, d, j] * c[t, j] for j in range(512))
+                acc += q[h, d] * k_d
+            for d in range(64):
+                acc += qr[d] * kr[t, d]
+            s.append(acc * scale)
+            vs.append([sum(wv[h, d, j] * c[t, j] for j in range(512)) for d in range(128)])
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        z = sum(e)
+        o = [sum(e[t] / z * vs[t][d] for t in range(L)) for d in range(128)]
+        out.append((o, m + math.log(z)))
+    return out
+
+
+def test_explicit_matches_scalar_bruteforce():
+    rng = np.random.default_rng(5)
+    q, c, kr, wk, wv = _rand_case(rng, n_h=2, L=3)
+    r = M.attend_explicit(q, c, kr, wk, wv, pos_q=7)
+    bf = _scalar_loop_attention(q, c, kr, wk, wv, 7, M.default_scale())
+    for h, (o, lse) in enumerate(bf):
+        np.testing.assert_allclose(r["o"][h], o, rtol=1e-11, atol=1e-13)
+        assert r["lse"][h] == pytest.approx(lse, rel=1e-12)
+
+
+def test_softmax_rows_sum_to_one():
+    rng = np.random.default_rng(6)
+    q, c, kr, wk, wv = _rand_case(rng, n_h=4, L=50)
+    r = M.attend_explicit(q * 5, c, kr, wk, wv, pos_q=49, return_p=True)
+    assert np.all(r["p"] >= 0)
+    np.testing.assert_allclose(r["p"].sum(axis=1), 1.0, atol=1e-12)
+
+
+def test_length_one_returns_that_tokens_value():
+    rng = np.random.default_rng(7)
+    q, c, kr, wk, wv = _rand_case(rng, n_h=4, L=1)
+    r = M.attend_explicit(q, c, kr, wk, wv, pos_q=0)
+    for h in range(4):
+        np.testing.assert_allclose(r["o"][h], wv[h] @ c[0], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(r["o_lat"][h], c[0], rtol=1e-13, atol=1e-14)
+
+
+def test_constant_cache_returns_projected_row():
+    rng = np.random.default_rng(8)
+    q, c, kr, wk, wv = _rand_case(rng, n_h=3, L=9)
+    c[:] = c[0]
+    kr[:] = kr[0]
+    r = M.attend_explicit(q, c, kr, wk, wv, pos_q=8)
+    for h in range(3):
+        np.testing.assert_allclose(r["o"][h], wv[h] @ c[0], rtol=1e-12, atol=1e-14)
+        assert r["lse"][h] == pytest.approx(
+            (np.concatenate([wk[h] @ c[0], kr[0]]) @ np.concatenate(
+                [q[h, :128], M.rope(q[h, 128:], 8)])) * M.default_scale() + math.log(9), rel=1e-12)
+
+
+def test_zero_query_gives_uniform_weights():
+    rng = np.random.default_rng(9)
+    _, c, kr, wk, wv = _rand_case(rng, n_h=2, L=33)
+    q = np.zeros((2, 192))
+    r = M.attend_explicit(q, c, kr, wk, wv, pos_q=32)
+    np.testing.assert_allclose(r["o_lat"], np.broadcast_to(c.mean(axis=0), (2, 512)), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r["lse"], math.log(33), rtol=1e-14)
+
+
+def test_two_token_closed_form_pins_scale_and_orientation():
+    # Token 0 is all zeros; token 1 has latent e_k and RoPE key e_j.
+    # s_0 = 0 and s_1 = scale·(q^C·W_UK[h][:, k] + q^R'_j), so p_1 = sigmoid(s_1),
+    # o = p_1·W_UV[h][:, k] and o^lat = p_1·e_k.
+    rng = np.random.default_rng(10)
+    n_h, k, j = 2, 37, 11
+    wk = rng.standard_normal((n_h, 128, 512)) / math.sqrt(512)
+    wv = rng.standard_normal((n_h, 128, 512)) / math.sqrt(512)
+    q = rng.standard_normal((n_h, 192))
+    c = np.zeros((2, 512)); c[1, k] = 1.0
+    kr = np.zeros((2, 64)); kr[1, j] = 1.0
+    r = M.attend_explicit(q, c, kr, wk, wv, pos_q=0)     # position 0: no rotation
+    scale = 1.0 / math.sqrt(192.0)
+    for h in range(n_h):
+        s1 = scale * (q[h, :128] @ wk[h][:, k] + q[h, 128 + j])
+        p1 = 1.0 / (1.0 + math.exp(-s1))
+        np.testing.assert_allclose(r["o"][h], p1 * wv[h][:, k], rtol=1e-12, atol=1e-15)
+        assert r["o_lat"][h, k] == pytest.approx(p1, rel=1e-12)
+        assert r["lse"][h] == pytest.approx(math.log(1.0 + math.exp(s1)), rel=1e-12)
+
+
+def test_empty_context():
+    rng = np.random.default_rng(11)
+    q, c, kr, wk, wv = _rand_case(rng, n_h=2, L=0)
+    r = M.attend_explicit(q, c, kr, wk, wv, pos_q=0)
+    assert np.all(r["o"] == 0) and np.all(r["o_lat"] == 0)
+    assert np.all(np.isneginf(r["lse"]))
+
+
+def test_merge_of_disjoint_parts_equals_whole():
+    rng = np.random.default_rng(12)
+    q, c, kr, wk, wv = _rand_case(rng, n_h=3, L=40)
+    whole = M.attend_explicit(q, c, kr, wk, wv, pos_q=39)
+    cuts = [0, 7, 7, 23, 40]          # includes an empty part
+    parts = [M.attend_explicit(q, c[a:b], kr[a:b], wk, wv, pos_q=39) for a, b in zip(cuts[:-1], cuts[1:])]
+    o, lse = M.merge_partials(np.stack([p["o_lat"] for p in parts]), np.stack([p["lse"] for p in parts]))
+    np.testing.assert_allclose(o, whole["o_lat"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, whole["lse"], rtol=1e-13)
+    # all parts empty → zero output, -inf lse
+    o0, l0 = M.merge_partials(np.zeros((2, 3, 512)), np.full((2, 3), -np.inf))
+    assert np.all(o0 == 0) and np.all(np.isneginf(l0))
+
+
+# --------------------------- cache-size arithmetic --------------------------------
+def test_cache_size_matches_the_pages():
+    g = json.load(open(os.path.join(HERE, "golden", "cache_arithmetic.json")))
+    assert M.mla_cache_elements(g["d_c"], g["d_rope"], 1) == g["row_elements"] == M.D_ROW
+    assert M.mha_cache_elements(g["n_heads"], M.D_H, 1) == 32768
+    assert M.gqa_equivalent_groups(g["d_c"], g["d_rope"], M.D_H) == g["gqa_groups"]
+    b1 = M.mla_cache_bytes(g["d_c"], g["d_rope"], g["layers"], g["context_tokens"], 1,
+                           g["avg_bits_per_element"]) / 1e9
+    b64 = M.mla_cache_bytes(g["d_c"], g["d_rope"], g["layers"], g["context_tokens"], 64,
+                            g["avg_bits_per_element"]) / 1e9
+    assert abs(b1 - g["cache_gb_batch1_printed"]) <= g["printed_precision_gb"]["batch1"]
+    assert abs(b64 - g["cache_gb_batch64_printed"]) <= g["printed_precision_gb"]["batch64"]
