@@ -1,0 +1,193 @@
+/*
+ * mla.h — C ABI of the B300 (sm_103a) MLA latent-cache decode library.
+ *
+ * One decode step of one Multi-head Latent Attention (MLA) layer over its
+ * compressed KV cache. Every cached token holds a 512-wide latent c_KV plus a
+ * shared 64-wide decoupled RoPE key k^R: 576 elements per token per layer.
+ *   "DeepSeek-V2 机制拆解：KV 缓存压缩 93.3% 是怎么做到的" (discosf.com),
+ *     §"长上下文推理的第一瓶颈": decode re-reads every previous token's K/V; only
+ *     the d_c = 512 latent is cached and K/V are up-projected from it; W_UK can
+ *     be absorbed into the query side and W_UV into the output side.
+ *   Same page, §"解耦 RoPE 与 YaRN": RoPE is carried by a decoupled per-head query
+ *     and a shared key of width 64 so that absorption survives.
+ *   "DeepSeek-V2: A Strong, Economical, and Efficient Mixture-of-Experts Language
+ *     Model - 中文验证版" (ai-papers.xuzou.cn), §"瓶颈" and §"方法适配": cache
+ *     formula (d_c + d_h^R)·l, d_c = 512, d_h^R = 64, 128 heads.
+ *
+ * The step is four calls on the caller's stream:
+ *   mla_absorb_q   q_lat[b,h] = [ W_UK[h]^T q^C[b,h]  ‖  RoPE(q^R[b,h], pos[b]) ]
+ *   mla_decode_fwd split-KV attention of every head over the 576-wide cache rows
+ *   mla_combine    log-sum-exp merge of the per-split partial results
+ *   mla_up_v       o[b,h] = W_UV[h] o_lat[b,h]
+ *
+ * Conventions shared by every call
+ *   - All pointers except `cache` (a host struct) are DEVICE pointers; the caller
+ *     allocates and owns every buffer. The library allocates nothing, keeps no
+ *     state beyond a per-device attribute cache, and never synchronises the stream.
+ *   - Tensors are dense row-major with the shapes given; base addresses must be
+ *     16-byte aligned.
+ *   - bf16 means IEEE bfloat16 stored as 16-bit words.
+ *   - Arguments are validated on the host before any CUDA call; a bad argument
+ *     returns MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED and launches nothing.
+ *     A launch failure reported by the runtime returns MLA_ERR_CUDA.
+ *   - Problems only the device can see (a page id outside the pool, a bounded
+ *     wait that ran out) are written to the optional device status word
+ *     (first error wins; the caller zeroes it) and the affected work is skipped.
+ *   - Fixed widths: d_h = 128 (q^C), d_h^R = 64, d_c = 512, row = 576.
+ *     n_h must be 16, 32, 64 or 128.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#define MLA_ABI_VERSION 1
+#define MLA_D_NOPE 128
+#define MLA_D_ROPE 64
+#define MLA_D_LATENT 512
+#define MLA_D_ROW 576
+#define MLA_D_Q 192
+#define MLA_PAGE_SIZE 64
+#define MLA_MAX_SPLITS 256
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size          */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. n_h = 96)  */
+  MLA_ERR_WORKSPACE = 3,     /* a size/limit of a caller buffer exceeded   */
+  MLA_ERR_CUDA = 4,          /* the CUDA runtime reported an error         */
+  MLA_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up             */
+  MLA_ERR_DEVICE_BOUNDS = 6  /* device: a page id fell outside the pool    */
+} mla_status;
+
+typedef enum mla_kv_dtype {
+  MLA_KV_BF16 = 0,      /* rows of 576 bf16 (1152 bytes)                      */
+  MLA_KV_FP8_E4M3 = 1   /* rows of 576 e4m3 codes (576 bytes) + fp32 scale    */
+} mla_kv_dtype;
+
+/*
+ * View of one layer's latent cache (host struct; the pointers inside are device
+ * memory owned by the caller). Token t of sequence b lives in row
+ *   contiguous (block_table == NULL): b * seq_stride_tokens + t
+ *   paged      (block_table != NULL): block_table[b * max_pages + t / 64] * 64 + t % 64
+ * Row r starts at byte r * 1152 (bf16) or r * 576 (e4m3) of `data`; columns
+ * 0..511 are c_KV and 512..575 the RoPE key, stored already rotated at t.
+ * For e4m3 the token's value is code * scales[r] (one fp32 scale per row).
+ * Rows in [L_b, ...) of a sequence's last page are never used for attention.
+ */
+typedef struct mla_cache {
+  int32_t dtype;                /* mla_kv_dtype                                   */
+  int32_t page_size;            /* must be 64 when block_table != NULL            */
+  const void* data;             /* device rows                                    */
+  const float* scales;          /* device [num_rows] fp32 (e4m3 only), else NULL  */
+  const int32_t* block_table;   /* device [B, max_pages] page ids, or NULL        */
+  int32_t max_pages;            /* row stride of block_table (entries)            */
+  int32_t reserved;             /* must be 0                                      */
+  int64_t seq_stride_tokens;    /* contiguous only: rows between sequences        */
+  int64_t num_rows;             /* rows addressable through data (bounds checks)  */
+} mla_cache;
+
+/*
+ * mla_absorb_q — fold W_UK into the query and rotate the decoupled query part.
+ *   ("DeepSeek-V2 机制拆解", §"长上下文推理的第一瓶颈" (absorption) and
+ *    §"解耦 RoPE 与 YaRN" (decoupled RoPE).)
+ *   q     [B, n_h, 192] bf16: q^C = q[..., 0:128], q^R = q[..., 128:192]
+ *   w_uk  [n_h, 128, 512] bf16 (K_h = W_UK[h] · c)
+ *   pos   [B] int32 query position (>= 0), normally L_b - 1
+ *   q_lat [B, n_h, 576] bf16 out:
+ *         q_lat[b,h,j]       = sum_d q^C[b,h,d] W_UK[h,d,j]          (j < 512)
+ *         q_lat[b,h,512 + i] = rotate-half RoPE of q^R[b,h] at pos[b],
+ *                              pair (i, i+32), angle pos * rope_base^(-i/32)
+ *   Accumulation fp32, RoPE angles reduced in fp64, result rounded to bf16.
+ */
+MLA_API mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* pos,
+                        int B, int n_h, float rope_base, void* q_lat,
+                        cudaStream_t stream);
+
+/*
+ * mla_decode_fwd — split-KV attention of all heads over the latent cache.
+ *   Scores s[h,t] = softmax_scale * (q_lat[b,h,:] . row_t[0:576]), softmax over
+ *   the tokens of each split with a running maximum, and the value is the latent
+ *   itself: o_part = sum_t p[h,t] row_t[0:512] / sum_t p[h,t].
+ *   ("DeepSeek-V2 机制拆解", §"长上下文推理的第一瓶颈": with W_UK/W_UV absorbed,
+ *    all heads attend directly over the cached latent.)
+ *   q_lat      [B, n_h, 576] bf16
+ *   cache      host pointer to the cache view above
+ *   seq_lens   [B] int32 device, 0 <= L_b <= max_seq_len
+ *   max_seq_len host upper bound of seq_lens (sizes the launch)
+ *   num_splits S, 1..MLA_MAX_SPLITS, or 0 for mla_num_splits(B, max_seq_len, n_h)
+ *   o_part     [B, S, n_h, 512] fp32 out, normalised per split
+ *   lse_part   [B, S, n_h] fp32 out, natural-log normaliser of the split
+ *              (-inf, with o_part = 0, for a split that holds no token)
+ *   status     optional device int32 (may be NULL)
+ *   Split s of sequence b covers the tokens mla_split_range(L_b, S, s) returns.
+ */
+MLA_API mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache,
+                          const int32_t* seq_lens, int B, int n_h, int max_seq_len,
+                          float softmax_scale, int num_splits,
+                          float* o_part, float* lse_part, int32_t* status,
+                          cudaStream_t stream);
+
+/*
+ * mla_combine — merge split partials by log-sum-exp.
+ *   m = max_s lse[s];  w_s = exp(lse[s] - m);  o_lat = sum_s w_s o_part[s] / sum_s w_s;
+ *   lse = m + ln sum_s w_s.  Splits with lse = -inf weigh 0; if all are empty the
+ *   result is o_lat = 0, lse = -inf.
+ *   o_part [B, S, n_h, 512] fp32, lse_part [B, S, n_h] fp32
+ *   o_lat  [B, n_h, 512] fp32 out;  lse [B, n_h] fp32 out (may be NULL)
+ */
+MLA_API mla_status mla_combine(const float* o_part, const float* lse_part, int B,
+                       int num_splits, int n_h, float* o_lat, float* lse,
+                       cudaStream_t stream);
+
+/*
+ * mla_up_v — apply W_UV on the output side.
+ *   ("DeepSeek-V2 机制拆解", §"长上下文推理的第一瓶颈": V = W_UV · c, absorbed.)
+ *   o[b,h,d] = sum_j W_UV[h,d,j] o_lat[b,h,j]
+ *   o_lat [B, n_h, 512] fp32, w_uv [n_h, 128, 512] bf16, o [B, n_h, 128] fp32 out
+ *   (W_O, which would follow, is outside this library.)
+ */
+MLA_API mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h,
+                    float* o, cudaStream_t stream);
+
+/*
+ * mla_quantize_fp8 — cache-write helper: bf16 rows → e4m3 rows + per-row scale.
+ *   The pages report a low-bit KV cache for serving ("DeepSeek-V2 机制拆解",
+ *   §"推理参数与 128K 上下文的使用注意"; "中文验证版", §"方法适配") without its format;
+ *   this library's stand-in is e4m3 with one fp32 scale per token:
+ *   scale = amax/448 (amax = max |x| over the 576 elements; 1 for a zero row),
+ *   code  = e4m3(x / scale), fp32 division, round-to-nearest-even, saturating.
+ *   rows [num_rows, 576] bf16; codes [num_rows, 576] uint8 out; scales [num_rows] fp32 out
+ */
+MLA_API mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t* codes,
+                            float* scales, cudaStream_t stream);
+
+/* Split count num_splits = 0 resolves to (>= 1, <= MLA_MAX_SPLITS). Host only. */
+MLA_API int mla_num_splits(int B, int max_seq_len, int n_h);
+
+/*
+ * Token range [*start, *end) of split `split` of a sequence of seq_len tokens
+ * under num_splits splits: chunk = 64 * ceil(ceil(seq_len / 64) / num_splits),
+ * start = min(split * chunk, seq_len), end = min(start + chunk, seq_len).
+ * Host only; returns MLA_ERR_INVALID_ARG for bad arguments.
+ */
+MLA_API mla_status mla_split_range(int seq_len, int num_splits, int split, int* start, int* end);
+
+MLA_API const char* mla_status_string(int status);
+MLA_API int mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H_ */

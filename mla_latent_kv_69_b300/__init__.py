@@ -1,0 +1,208 @@
+"""B300-native (sm_103a) MLA latent-cache decode: Python binding of libmla_b300.so.
+
+The functions mirror the C ABI in include/mla.h one to one. They only marshal
+arguments (shape/dtype/device checks, raw pointers, the current CUDA stream);
+every step of the computation runs in the library's CUDA kernels. Buffers are
+torch tensors on the GPU; outputs are allocated here when not passed in.
+
+A decode step of one MLA layer:
+
+    q_lat = absorb_q(q, w_uk, pos)                      # [B, n_h, 576] bf16
+    o_part, lse_part = decode_fwd(q_lat, cache, seq_lens, max_seq_len)
+    o_lat, lse = combine(o_part, lse_part)              # [B, n_h, 512] fp32
+    o = up_v(o_lat, w_uv)                               # [B, n_h, 128] fp32
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaError, check,
+                   status_string)
+
+__all__ = [
+    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range",
+    "Cache", "MlaError", "status_string", "default_scale", "decode_step", "lib_path",
+]
+
+D_NOPE, D_ROPE, D_LATENT, D_ROW, D_Q, PAGE = 128, 64, 512, 576, 192, 64
+
+
+def lib_path() -> str:
+    return _lib.LIB_PATH
+
+
+def default_scale() -> float:
+    """1/sqrt(d_h + d_h^R) for the 192-wide query/key pair."""
+    return 1.0 / math.sqrt(D_NOPE + D_ROPE)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+@dataclass
+class Cache:
+    """One layer's latent cache (see mla_cache in include/mla.h).
+
+    data: contiguous [B, stride, 576] or paged [pages, 64, 576]; bf16 or uint8 (e4m3 codes)
+    scales: fp32 per row ([B, stride] or [pages, 64]) for e4m3, else None
+    block_table: int32 [B, max_pages] for paged, else None
+    """
+    data: torch.Tensor
+    scales: torch.Tensor | None = None
+    block_table: torch.Tensor | None = None
+
+    @property
+    def dtype_code(self) -> int:
+        return MLA_KV_FP8_E4M3 if self.data.dtype in (torch.uint8, torch.float8_e4m3fn) else MLA_KV_BF16
+
+    def to_c(self) -> MlaCache:
+        d = self.data
+        if d.dtype not in (torch.bfloat16, torch.uint8, torch.float8_e4m3fn):
+            raise TypeError("cache data must be bf16 or uint8/float8_e4m3fn codes")
+        if not d.is_cuda or not d.is_contiguous() or d.dim() != 3 or d.shape[-1] != D_ROW:
+            raise ValueError("cache data must be a contiguous CUDA tensor [*, *, 576]")
+        c = MlaCache()
+        c.dtype = self.dtype_code
+        c.data = d.data_ptr()
+        c.scales = _ptr(self.scales)
+        if self.scales is not None:
+            _need(self.scales, "scales", torch.float32)
+        c.num_rows = d.shape[0] * d.shape[1]
+        if self.block_table is not None:
+            _need(self.block_table, "block_table", torch.int32)
+            if d.shape[1] != PAGE:
+                raise ValueError("paged cache data must be [pages, 64, 576]")
+            c.block_table = self.block_table.data_ptr()
+            c.page_size = PAGE
+            c.max_pages = self.block_table.shape[1]
+        else:
+            c.block_table = None
+            c.seq_stride_tokens = d.shape[1]
+        return c
+
+
+def num_splits(B: int, max_seq_len: int, n_h: int) -> int:
+    return int(_lib.get().mla_num_splits(B, max_seq_len, n_h))
+
+
+def split_range(seq_len: int, n_splits: int, split: int) -> tuple[int, int]:
+    a, b = ctypes.c_int(), ctypes.c_int()
+    check("mla_split_range", _lib.get().mla_split_range(seq_len, n_splits, split, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def absorb_q(q, w_uk, pos, q_lat=None, rope_base: float = 10000.0, stream=None):
+    B, n_h = q.shape[0], q.shape[1]
+    _need(q, "q", torch.bfloat16, (B, n_h, D_Q))
+    _need(w_uk, "w_uk", torch.bfloat16, (n_h, D_NOPE, D_LATENT))
+    _need(pos, "pos", torch.int32, (B,))
+    if q_lat is None:
+        q_lat = torch.empty(B, n_h, D_ROW, dtype=torch.bfloat16, device=q.device)
+    _need(q_lat, "q_lat", torch.bfloat16, (B, n_h, D_ROW))
+    check("mla_absorb_q", _lib.get().mla_absorb_q(_ptr(q), _ptr(w_uk), _ptr(pos), B, n_h, float(rope_base),
+                                                _ptr(q_lat), _stream(stream)))
+    return q_lat
+
+
+def decode_fwd(q_lat, cache: Cache, seq_lens, max_seq_len: int, softmax_scale: float | None = None,
+               n_splits: int = 0, o_part=None, lse_part=None, status=None, stream=None):
+    B, n_h = q_lat.shape[0], q_lat.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, (B, n_h, D_ROW))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    S = n_splits if n_splits > 0 else num_splits(B, max_seq_len, n_h)
+    if o_part is None:
+        o_part = torch.empty(B, S, n_h, D_LATENT, dtype=torch.float32, device=q_lat.device)
+    if lse_part is None:
+        lse_part = torch.empty(B, S, n_h, dtype=torch.float32, device=q_lat.device)
+    _need(o_part, "o_part", torch.float32, (B, S, n_h, D_LATENT))
+    _need(lse_part, "lse_part", torch.float32, (B, S, n_h))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    c = cache.to_c()
+    scale = default_scale() if softmax_scale is None else float(softmax_scale)
+    check("mla_decode_fwd", _lib.get().mla_decode_fwd(
+        _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale, S,
+        _ptr(o_part), _ptr(lse_part), _ptr(status), _stream(stream)))
+    return o_part, lse_part
+
+
+def combine(o_part, lse_part, o_lat=None, lse=None, stream=None):
+    B, S, n_h = o_part.shape[0], o_part.shape[1], o_part.shape[2]
+    _need(o_part, "o_part", torch.float32, (B, S, n_h, D_LATENT))
+    _need(lse_part, "lse_part", torch.float32, (B, S, n_h))
+    if o_lat is None:
+        o_lat = torch.empty(B, n_h, D_LATENT, dtype=torch.float32, device=o_part.device)
+    if lse is None:
+        lse = torch.empty(B, n_h, dtype=torch.float32, device=o_part.device)
+    _need(o_lat, "o_lat", torch.float32, (B, n_h, D_LATENT))
+    _need(lse, "lse", torch.float32, (B, n_h))
+    check("mla_combine", _lib.get().mla_combine(_ptr(o_part), _ptr(lse_part), B, S, n_h, _ptr(o_lat), _ptr(lse),
+                                              _stream(stream)))
+    return o_lat, lse
+
+
+def up_v(o_lat, w_uv, o=None, stream=None):
+    B, n_h = o_lat.shape[0], o_lat.shape[1]
+    _need(o_lat, "o_lat", torch.float32, (B, n_h, D_LATENT))
+    _need(w_uv, "w_uv", torch.bfloat16, (n_h, D_NOPE, D_LATENT))
+    if o is None:
+        o = torch.empty(B, n_h, D_NOPE, dtype=torch.float32, device=o_lat.device)
+    _need(o, "o", torch.float32, (B, n_h, D_NOPE))
+    check("mla_up_v", _lib.get().mla_up_v(_ptr(o_lat), _ptr(w_uv), B, n_h, _ptr(o), _stream(stream)))
+    return o
+
+
+def quantize_fp8(rows, codes=None, scales=None, stream=None):
+    """rows [..., 576] bf16 → (codes uint8 [..., 576], scales fp32 [...])."""
+    if rows.dtype != torch.bfloat16 or rows.shape[-1] != D_ROW:
+        raise TypeError("rows must be bf16 [..., 576]")
+    lead = tuple(rows.shape[:-1])
+    n = int(math.prod(lead))
+    if codes is None:
+        codes = torch.empty(*lead, D_ROW, dtype=torch.uint8, device=rows.device)
+    if scales is None:
+        scales = torch.empty(*lead, dtype=torch.float32, device=rows.device)
+    _need(rows, "rows", torch.bfloat16)
+    _need(codes, "codes", torch.uint8, (*lead, D_ROW))
+    _need(scales, "scales", torch.float32, lead)
+    check("mla_quantize_fp8", _lib.get().mla_quantize_fp8(_ptr(rows), n, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def decode_step(q, w_uk, w_uv, cache: Cache, seq_lens, pos, max_seq_len: int, n_splits: int = 0,
+                softmax_scale: float | None = None, rope_base: float = 10000.0, bufs: dict | None = None,
+                status=None, stream=None):
+    """All four calls of one decode step; `bufs` (optional) holds preallocated outputs."""
+    bufs = {} if bufs is None else bufs
+    q_lat = absorb_q(q, w_uk, pos, q_lat=bufs.get("q_lat"), rope_base=rope_base, stream=stream)
+    o_part, lse_part = decode_fwd(q_lat, cache, seq_lens, max_seq_len, softmax_scale, n_splits,
+                                  o_part=bufs.get("o_part"), lse_part=bufs.get("lse_part"), status=status,
+                                  stream=stream)
+    o_lat, lse = combine(o_part, lse_part, o_lat=bufs.get("o_lat"), lse=bufs.get("lse"), stream=stream)
+    o = up_v(o_lat, w_uv, o=bufs.get("o"), stream=stream)
+    return dict(q_lat=q_lat, o_part=o_part, lse_part=lse_part, o_lat=o_lat, lse=lse, o=o)

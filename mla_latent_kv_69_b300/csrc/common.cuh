@@ -1,0 +1,87 @@
+// Shared device/host helpers for the MLA decode library (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kNope = MLA_D_NOPE;      // 128
+constexpr int kRope = MLA_D_ROPE;      // 64
+constexpr int kLatent = MLA_D_LATENT;  // 512
+constexpr int kRow = MLA_D_ROW;        // 576
+constexpr int kQ = MLA_D_Q;            // 192
+constexpr int kPage = MLA_PAGE_SIZE;   // 64
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Token range of split `s` (of S) of a sequence of L tokens: chunks are whole
+// 64-token tiles, front-loaded; trailing splits may be empty.
+__host__ __device__ inline void split_range(int L, int S, int s, int* start, int* end) {
+  int tiles = ceil_div(L, kPage);
+  int chunk = kPage * ceil_div(tiles, S);
+  int64_t st = (int64_t)s * chunk;
+  if (st > L) st = L;
+  int64_t en = st + chunk;
+  if (en > L) en = L;
+  *start = (int)st;
+  *end = (int)en;
+}
+
+// First device-side error wins.
+__device__ inline void record_status(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Everything a decode kernel needs, resolved on the host.
+struct DecodeParams {
+  const __nv_bfloat16* q_lat;   // [B, n_h, 576]
+  const void* data;             // cache rows
+  const float* scales;          // fp8 per-row scales or nullptr
+  const int32_t* block_table;   // [B, max_pages] or nullptr
+  const int32_t* seq_lens;      // [B]
+  float* o_part;                // [B, S, n_h, 512]
+  float* lse_part;              // [B, S, n_h]
+  int32_t* status;
+  int64_t seq_stride;           // contiguous row stride between sequences
+  int64_t num_rows;             // addressable rows
+  int32_t max_pages;
+  int32_t kv_dtype;             // mla_kv_dtype
+  int32_t B, n_h, S;
+  float scale;                  // softmax scale (natural-log units)
+};
+
+// Row index of token t (>= 0) of sequence b, or -1 when the token falls outside the
+// caller's buffers (a page id outside the pool, or a length beyond the block table
+// or the contiguous stride).
+__device__ inline int64_t cache_row(const DecodeParams& p, int b, int t) {
+  if (p.block_table == nullptr) {
+    if (t >= p.seq_stride) return -1;
+    const int64_t row = (int64_t)b * p.seq_stride + t;
+    return row < p.num_rows ? row : -1;
+  }
+  if ((t >> 6) >= p.max_pages) return -1;
+  const int32_t page = p.block_table[(int64_t)b * p.max_pages + (t >> 6)];
+  const int64_t row = (int64_t)page * kPage + (t & (kPage - 1));
+  if (page < 0 || row >= p.num_rows) return -1;
+  return row;
+}
+
+// Host-side launchers (one per kernel family); each returns the launch error.
+cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const int32_t* pos,
+                            int B, int n_h, float rope_base, __nv_bfloat16* q_lat, cudaStream_t st);
+cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, int n_h, float* o,
+                        cudaStream_t st);
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int S, int n_h,
+                           float* o_lat, float* lse, cudaStream_t st);
+cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t n, uint8_t* codes, float* scales,
+                                cudaStream_t st);
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t st);
+
+}  // namespace mla

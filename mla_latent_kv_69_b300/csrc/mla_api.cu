@@ -1,0 +1,169 @@
+// The library's extern "C" boundary: host-side validation, then one launch per call
+// on the caller's stream. Validation touches no CUDA API, so a rejected call has no
+// side effect and works without a GPU.
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "decode_tc.cuh"
+
+namespace {
+
+using namespace mla;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool valid_heads(int n_h) { return n_h == 16 || n_h == 32 || n_h == 64 || n_h == 128; }
+inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+constexpr int kMaxBatch = 65535;   // grid dimensions carry B
+
+// Per-device SM count, queried once per device.
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 148;
+  }
+  std::lock_guard<std::mutex> g(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 148;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument (null, misaligned or out-of-range)";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: valid but unsupported configuration";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: caller buffer too small or a fixed limit exceeded";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: the CUDA runtime reported an error";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case MLA_ERR_DEVICE_BOUNDS: return "MLA_ERR_DEVICE_BOUNDS: a page id fell outside the cache pool";
+    default: return "unknown mla_status";
+  }
+}
+
+mla_status mla_split_range(int seq_len, int num_splits, int split, int* start, int* end) {
+  if (!start || !end || seq_len < 0 || num_splits < 1 || num_splits > MLA_MAX_SPLITS || split < 0 ||
+      split >= num_splits)
+    return MLA_ERR_INVALID_ARG;
+  split_range(seq_len, num_splits, split, start, end);
+  return MLA_OK;
+}
+
+int mla_num_splits(int B, int max_seq_len, int n_h) {
+  if (B < 1 || max_seq_len < 0 || !valid_heads(n_h)) return 1;
+  const int tiles = ceil_div(max_seq_len, kPage);
+  if (tiles <= 1) return 1;
+  return decode_tc_num_splits(B, tiles, n_h, sm_count());
+}
+
+mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* pos, int B, int n_h,
+                        float rope_base, void* q_lat, cudaStream_t stream) {
+  if (!q || !w_uk || !pos || !q_lat) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(w_uk) || !aligned16(q_lat) || !aligned16(pos)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxBatch) return MLA_ERR_INVALID_ARG;
+  if (!valid_heads(n_h)) return n_h > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (!(rope_base > 1.f) || !std::isfinite(rope_base)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_absorb_q(static_cast<const __nv_bfloat16*>(q),
+                                     static_cast<const __nv_bfloat16*>(w_uk), pos, B, n_h, rope_base,
+                                     static_cast<__nv_bfloat16*>(q_lat), stream));
+}
+
+mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens, int B,
+                          int n_h, int max_seq_len, float softmax_scale, int num_splits, float* o_part,
+                          float* lse_part, int32_t* status, cudaStream_t stream) {
+  if (!q_lat || !cache || !seq_lens || !o_part || !lse_part) return MLA_ERR_INVALID_ARG;
+  if (!cache->data || cache->reserved != 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_lat) || !aligned16(cache->data) || !aligned16(o_part) || !aligned16(lse_part) ||
+      !aligned16(seq_lens))
+    return MLA_ERR_INVALID_ARG;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxBatch) return MLA_ERR_INVALID_ARG;
+  if (!valid_heads(n_h)) return n_h > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (max_seq_len < 0 || max_seq_len > (INT_MAX / 2)) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (cache->dtype == MLA_KV_BF16) {
+    if (cache->scales) return MLA_ERR_INVALID_ARG;
+  } else if (cache->dtype == MLA_KV_FP8_E4M3) {
+    if (!cache->scales || !aligned16(cache->scales)) return MLA_ERR_INVALID_ARG;
+  } else {
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (cache->num_rows < 0) return MLA_ERR_INVALID_ARG;
+  if (cache->block_table) {
+    if (cache->page_size != kPage) return cache->page_size > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+    if (!aligned16(cache->block_table)) return MLA_ERR_INVALID_ARG;
+    if (cache->max_pages < ceil_div(max_seq_len, kPage) || cache->max_pages < 1) return MLA_ERR_INVALID_ARG;
+    if (cache->num_rows % kPage) return MLA_ERR_INVALID_ARG;
+  } else {
+    if (cache->seq_stride_tokens < max_seq_len) return MLA_ERR_INVALID_ARG;
+    if (cache->num_rows < (int64_t)(B - 1) * cache->seq_stride_tokens + max_seq_len) return MLA_ERR_INVALID_ARG;
+  }
+  const int S = num_splits == 0 ? mla_num_splits(B, max_seq_len, n_h) : num_splits;
+
+  DecodeParams p{};
+  p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+  p.data = cache->data;
+  p.scales = cache->scales;
+  p.block_table = cache->block_table;
+  p.seq_lens = seq_lens;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.status = status;
+  p.seq_stride = cache->seq_stride_tokens;
+  p.num_rows = cache->num_rows;
+  p.max_pages = cache->max_pages;
+  p.kv_dtype = cache->dtype;
+  p.B = B;
+  p.n_h = n_h;
+  p.S = S;
+  p.scale = softmax_scale;
+  if (decode_tc_supported(p)) return cuda_status(launch_decode_tc(p, max_seq_len, stream));
+  return cuda_status(launch_decode_simt(p, stream));
+}
+
+mla_status mla_combine(const float* o_part, const float* lse_part, int B, int num_splits, int n_h,
+                       float* o_lat, float* lse, cudaStream_t stream) {
+  if (!o_part || !lse_part || !o_lat) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxBatch || num_splits < 1 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (!valid_heads(n_h)) return n_h > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(o_part, lse_part, B, num_splits, n_h, o_lat, lse, stream));
+}
+
+mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h, float* o, cudaStream_t stream) {
+  if (!o_lat || !w_uv || !o) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxBatch) return MLA_ERR_INVALID_ARG;
+  if (!valid_heads(n_h)) return n_h > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_up_v(o_lat, static_cast<const __nv_bfloat16*>(w_uv), B, n_h, o, stream));
+}
+
+mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t* codes, float* scales,
+                            cudaStream_t stream) {
+  if (!rows || !codes || !scales) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(rows) || !aligned16(codes) || !aligned16(scales)) return MLA_ERR_INVALID_ARG;
+  if (num_rows < 0 || num_rows > ((int64_t)1 << 33)) return MLA_ERR_INVALID_ARG;
+  if (num_rows == 0) return MLA_OK;
+  return cuda_status(launch_quantize_fp8(static_cast<const __nv_bfloat16*>(rows), num_rows, codes, scales, stream));
+}
+
+}  // extern "C"

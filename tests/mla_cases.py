@@ -1,0 +1,70 @@
+"""Helpers for GPU tests: build a workload's device tensors from the seeded generator,
+run the library, and evaluate the oracle on chosen (sequence, head) samples."""
+
+from __future__ import annotations
+
+import numpy as np
+import workloads as W
+from oracle import fp8_e4m3, mla_oracle
+
+MAX_REL = 2e-2      # max|gpu - oracle| <= MAX_REL * max|oracle|
+MEAN_REL = 3e-3     # sum|gpu - oracle| / sum|oracle| <= MEAN_REL
+
+
+bits_to_torch_bf16 = W.bits_to_torch_bf16
+
+
+def rows_f32(bits: np.ndarray) -> np.ndarray:
+    return W.bf16_bits_to_f32(bits)
+
+
+class Case(W.DeviceInputs):
+    """A workload on the device, its cache in the library's format (e4m3 workloads are
+    quantised by the library's own cache writer), plus the oracle for any sequence."""
+
+    def __init__(self, w: W.Workload, device, lens=None, keep_rows: bool = False):
+        import mla_latent_kv_69_b300 as mla
+
+        super().__init__(w, device, lens=lens, keep_rows=keep_rows)
+        if w.kv == "fp8":
+            codes, scales = mla.quantize_fp8(self.source)
+            self.cache = mla.Cache(codes, scales, self.block_table)
+        else:
+            self.cache = mla.Cache(self.source, None, self.block_table)
+
+    def run(self, n_splits: int = 0, status=None, bufs=None):
+        import mla_latent_kv_69_b300 as mla
+
+        return mla.decode_step(self.q, self.w_uk, self.w_uv, self.cache, self.seq_lens, self.pos, self.max_len,
+                               n_splits=n_splits, status=status, bufs=bufs)
+
+    # ---------------- oracle side ----------------
+    def oracle_rows(self, b: int) -> np.ndarray:
+        """fp64 cache rows of sequence b as the oracle sees them."""
+        src = rows_f32(self.rows_of(b))
+        if self.w.kv == "fp8":
+            codes, scales = fp8_e4m3.quantize_rows(src)
+            return fp8_e4m3.dequantize_rows(codes, scales)
+        return src.astype(np.float64)
+
+    def oracle(self, b: int, heads=None):
+        rows = self.oracle_rows(b)
+        q = rows_f32(self.q_bits[b])
+        wk = rows_f32(self.wuk_bits)
+        wv = rows_f32(self.wuv_bits)
+        return mla_oracle.attend_explicit(q, rows[:, :512], rows[:, 512:], wk, wv, pos_q=int(self.pos_np[b]),
+                                          heads=heads)
+
+
+def tol_stats(got: np.ndarray, ref: np.ndarray) -> tuple[float, float]:
+    err = np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))
+    ref_abs = np.abs(np.asarray(ref, np.float64))
+    max_rel = err.max() / max(ref_abs.max(), 1e-300)
+    mean_rel = err.sum() / max(ref_abs.sum(), 1e-300)
+    return float(max_rel), float(mean_rel)
+
+
+def assert_within_tolerance(got, ref, what=""):
+    mx, mn = tol_stats(got, ref)
+    assert mx <= MAX_REL and mn <= MEAN_REL, f"{what}: max_rel={mx:.3e} mean_rel={mn:.3e}"
+    return mx, mn

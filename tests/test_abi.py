@@ -1,0 +1,128 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol include/mla.h
+declares, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_69_b300 as mla
+from mla_latent_kv_69_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INVALID, UNSUPPORTED = _lib.MLA_ERR_INVALID_ARG, _lib.MLA_ERR_UNSUPPORTED
+A = 0x10000          # a fake, 16-byte aligned "device" address (never dereferenced)
+MIS = A + 4          # misaligned
+
+
+def _declared():
+    hdr = open(os.path.join(ROOT, "include", "mla.h")).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", hdr)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.get()
+    names = _declared()
+    assert names == sorted(_lib.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.mla_abi_version() == 1
+
+
+def test_status_strings():
+    for s in range(7):
+        assert _lib.status_string(s).startswith("MLA_")
+    assert "unknown" in _lib.status_string(99)
+
+
+def test_split_range_rule():
+    # chunk = 64 * ceil(ceil(L/64)/S); splits are front-loaded, trailing ones may be empty
+    assert mla.split_range(4096, 3, 0) == (0, 1408)
+    assert mla.split_range(4096, 3, 2) == (2816, 4096)
+    assert mla.split_range(100, 4, 0) == (0, 64)
+    assert mla.split_range(100, 4, 1) == (64, 100)
+    assert mla.split_range(100, 4, 3) == (100, 100)
+    assert mla.split_range(0, 2, 1) == (0, 0)
+    for L in (1, 63, 64, 65, 1000, 131072):
+        for S in (1, 2, 5, 37):
+            covered = []
+            for s in range(S):
+                a, b = mla.split_range(L, S, s)
+                assert a <= b and (a == b or a % 64 == 0)
+                covered.extend(range(a, b))
+            assert covered == list(range(L))
+    with pytest.raises(mla.MlaError):
+        mla.split_range(10, 0, 0)
+    with pytest.raises(mla.MlaError):
+        mla.split_range(10, 2, 2)
+
+
+def test_num_splits_range():
+    for B, L, h in [(1, 256, 16), (32, 4096, 128), (4, 131072, 128), (64, 32768, 128), (128, 8192, 128)]:
+        S = mla.num_splits(B, L, h)
+        assert 1 <= S <= _lib.MLA_MAX_SPLITS
+    assert mla.num_splits(4, 0, 128) == 1
+
+
+def _cache(**kw):
+    c = _lib.MlaCache()
+    c.dtype, c.page_size, c.data, c.scales, c.block_table = 0, 0, A, None, None
+    c.max_pages, c.reserved, c.seq_stride_tokens, c.num_rows = 0, 0, 4096, 32 * 4096
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _decode(c=None, **kw):
+    args = dict(q_lat=A, seq_lens=A, B=32, n_h=128, max_len=4096, scale=0.07, S=2, o_part=A, lse_part=A,
+                status=None)
+    args.update(kw)
+    c = _cache() if c is None else c
+    return _lib.get().mla_decode_fwd(args["q_lat"], ctypes.byref(c), args["seq_lens"], args["B"], args["n_h"],
+                                     args["max_len"], args["scale"], args["S"], args["o_part"], args["lse_part"],
+                                     args["status"], None)
+
+
+def test_decode_rejects_bad_arguments_on_host():
+    assert _decode(q_lat=None) == INVALID
+    assert _decode(q_lat=MIS) == INVALID
+    assert _decode(o_part=None) == INVALID
+    assert _decode(B=0) == INVALID
+    assert _decode(n_h=96) == UNSUPPORTED
+    assert _decode(n_h=0) == INVALID
+    assert _decode(S=-1) == INVALID
+    assert _decode(S=_lib.MLA_MAX_SPLITS + 1) == INVALID
+    assert _decode(scale=0.0) == INVALID
+    assert _decode(scale=float("nan")) == INVALID
+    assert _decode(max_len=-1) == INVALID
+    assert _decode(status=A + 2) == INVALID
+    assert _decode(_cache(data=None)) == INVALID
+    assert _decode(_cache(dtype=7)) == INVALID
+    assert _decode(_cache(reserved=1)) == INVALID
+    assert _decode(_cache(scales=A)) == INVALID                     # bf16 with scales
+    assert _decode(_cache(dtype=1)) == INVALID                      # fp8 without scales
+    assert _decode(_cache(dtype=1, scales=MIS)) == INVALID
+    assert _decode(_cache(seq_stride_tokens=100)) == INVALID        # stride < max_seq_len
+    assert _decode(_cache(num_rows=1000)) == INVALID                # rows do not cover the batch
+    paged = dict(block_table=A, page_size=64, max_pages=64, num_rows=64 * 100)
+    assert _decode(_cache(**{**paged, "page_size": 32})) == UNSUPPORTED
+    assert _decode(_cache(**{**paged, "max_pages": 10})) == INVALID   # too few pages for max_seq_len
+    assert _decode(_cache(**{**paged, "num_rows": 64 * 100 + 3})) == INVALID
+    assert _decode(_cache(**{**paged, "block_table": MIS})) == INVALID
+
+
+def test_other_calls_reject_bad_arguments_on_host():
+    L = _lib.get()
+    assert L.mla_absorb_q(None, A, A, 1, 128, 10000.0, A, None) == INVALID
+    assert L.mla_absorb_q(A, A, A, 1, 128, 0.5, A, None) == INVALID
+    assert L.mla_absorb_q(A, A, A, 1, 48, 10000.0, A, None) == UNSUPPORTED
+    assert L.mla_absorb_q(A, MIS, A, 1, 128, 10000.0, A, None) == INVALID
+    assert L.mla_combine(A, A, 1, 0, 128, A, None, None) == INVALID
+    assert L.mla_combine(A, A, 0, 1, 128, A, None, None) == INVALID
+    assert L.mla_combine(A, A, 1, 1, 128, None, None, None) == INVALID
+    assert L.mla_up_v(A, A, 1, 100, A, None) == UNSUPPORTED
+    assert L.mla_up_v(A, None, 1, 128, A, None) == INVALID
+    assert L.mla_quantize_fp8(A, -1, A, A, None) == INVALID
+    assert L.mla_quantize_fp8(MIS, 10, A, A, None) == INVALID
+    assert L.mla_quantize_fp8(A, 0, A, A, None) == _lib.MLA_OK      # nothing to do

@@ -186,3 +186,57 @@ def cache_bytes(w: Workload, lens=None) -> int:
     tokens = int(np.sum(lens, dtype=np.int64))
     per_tok = D_ROW * 2 if w.kv == "bf16" else D_ROW + 4
     return tokens * per_tok
+
+
+# ------------------------------ device upload ---------------------------------------
+def bits_to_torch_bf16(bits: np.ndarray, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class DeviceInputs:
+    """A workload's inputs uploaded to one device (torch tensors): q, w_uk, w_uv,
+    pos, seq_lens, the bf16 cache rows `source` (contiguous [B, stride, 576] or
+    paged [pages, 64, 576]) and the block table. Rows of each generated sequence
+    are kept on the host when keep_rows is set."""
+
+    def __init__(self, w: Workload, device, lens=None, keep_rows: bool = False):
+        import torch
+
+        self.w = w
+        self.device = device
+        self.lens = np.asarray(seq_lens(w) if lens is None else lens, dtype=np.int32)
+        self.B, self.n_h = w.batch, w.n_h
+        self.max_len = int(self.lens.max()) if len(self.lens) else 0
+        self.q_bits, self.wuk_bits, self.wuv_bits = gen_q(w), gen_w_uk(w), gen_w_uv(w)
+        self.q = bits_to_torch_bf16(self.q_bits, device)
+        self.w_uk = bits_to_torch_bf16(self.wuk_bits, device)
+        self.w_uv = bits_to_torch_bf16(self.wuv_bits, device)
+        self.pos_np = positions(self.lens)
+        self.pos = torch.from_numpy(self.pos_np).to(device)
+        self.seq_lens = torch.from_numpy(self.lens).to(device)
+        self.rows = {}
+        if w.paged:
+            self.block_table_np, self.pool_pages = gen_block_table(w, self.lens)
+            rows = [gen_rows(w, b, int(L)) for b, L in enumerate(self.lens)]
+            if keep_rows:
+                self.rows = dict(enumerate(rows))
+            self.source = bits_to_torch_bf16(layout_paged(rows, self.block_table_np, self.pool_pages), device)
+            del rows
+            self.block_table = torch.from_numpy(self.block_table_np).to(device)
+        else:
+            self.block_table_np, self.block_table, self.pool_pages = None, None, 0
+            stride = max(self.max_len, 1)
+            self.source = torch.zeros(self.B, stride, D_ROW, dtype=torch.bfloat16, device=device)
+            for b, L in enumerate(self.lens):
+                r = gen_rows(w, b, int(L))
+                if keep_rows:
+                    self.rows[b] = r
+                if L:
+                    self.source[b, :L] = bits_to_torch_bf16(r, device)
+
+    def rows_of(self, b: int) -> np.ndarray:
+        if b not in self.rows:
+            self.rows[b] = gen_rows(self.w, b, int(self.lens[b]))
+        return self.rows[b]
