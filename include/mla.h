@@ -173,6 +173,14 @@ MLA_API mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h
 MLA_API mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t* codes,
                             float* scales, cudaStream_t stream);
 
+/* Decode kernels (mla_decode_kernel's answer). */
+#define MLA_KERNEL_SIMT_F32 0   /* CUDA-core kernel, fp32 arithmetic                     */
+#define MLA_KERNEL_TC_BF16 1    /* tcgen05 tensor-core kernel, bf16 operands, fp32 accum.*/
+
+/* Which decode kernel mla_decode_fwd runs for this cache dtype and head count
+ * (-1 for an invalid combination). Host only. */
+MLA_API int mla_decode_kernel(int kv_dtype, int n_h);
+
 /* Split count num_splits = 0 resolves to (>= 1, <= MLA_MAX_SPLITS). Host only. */
 MLA_API int mla_num_splits(int B, int max_seq_len, int n_h);
 

@@ -25,7 +25,8 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaEr
                    status_string)
 
 __all__ = [
-    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range",
+    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range", "decode_kernel",
+    "compute_dtype",
     "Cache", "MlaError", "status_string", "default_scale", "decode_step", "lib_path",
 ]
 
@@ -104,6 +105,17 @@ class Cache:
             c.block_table = None
             c.seq_stride_tokens = d.shape[1]
         return c
+
+
+def decode_kernel(kv: str, n_h: int) -> str:
+    """Name of the decode kernel the library runs for a cache dtype ("bf16"/"fp8") and head count."""
+    code = int(_lib.get().mla_decode_kernel(MLA_KV_FP8_E4M3 if kv == "fp8" else MLA_KV_BF16, n_h))
+    return {0: "simt_f32", 1: "tcgen05_bf16"}.get(code, "invalid")
+
+
+def compute_dtype(n_h: int, kv: str) -> str:
+    """Arithmetic type of the decode kernel's contractions."""
+    return {"simt_f32": "f32", "tcgen05_bf16": "bf16"}.get(decode_kernel(kv, n_h), "?")
 
 
 def num_splits(B: int, max_seq_len: int, n_h: int) -> int:

@@ -24,7 +24,7 @@ MLA_MAX_SPLITS = 256
 
 EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
-    "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version",
+    "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version", "mla_decode_kernel",
 ]
 
 
@@ -61,11 +61,12 @@ def _load():
     lib.mla_up_v.argtypes = [vp, vp, i32, i32, vp, vp]
     lib.mla_quantize_fp8.argtypes = [vp, i64, vp, vp, vp]
     lib.mla_num_splits.argtypes = [i32, i32, i32]
+    lib.mla_decode_kernel.argtypes = [i32, i32]
     lib.mla_split_range.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
     lib.mla_status_string.argtypes = [i32]
     lib.mla_status_string.restype = ctypes.c_char_p
     for fn in ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
-               "mla_num_splits", "mla_split_range", "mla_abi_version"):
+               "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 

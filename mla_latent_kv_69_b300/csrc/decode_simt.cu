@@ -1,7 +1,7 @@
-// Scalar (CUDA-core, fp32) split-KV decode over the latent cache. It fixes every
-// layout and convention of mla_decode_fwd (row addressing, splits, masking, fp8
-// scales, outputs) in the plainest GPU form. It serves head counts below 128 and
-// is the GPU-side cross-check of the tensor-core kernel.
+// Scalar (CUDA-core, fp32) split-KV decode over the latent cache. It implements every
+// convention of mla_decode_fwd (row addressing, splits, masking, e4m3 scales, outputs)
+// in the plainest GPU form, and serves the configurations the tensor-core kernel
+// does not (mla_decode_kernel reports which one runs).
 //
 // Per block: one (split, sequence, group of 16 heads). Tiles of 32 tokens are staged
 // in shared memory as fp32; scores, an online softmax with a running maximum, and

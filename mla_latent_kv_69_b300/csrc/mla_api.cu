@@ -66,6 +66,15 @@ mla_status mla_split_range(int seq_len, int num_splits, int split, int* start, i
   return MLA_OK;
 }
 
+int mla_decode_kernel(int kv_dtype, int n_h) {
+  if (!valid_heads(n_h) || (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)) return -1;
+  DecodeParams p{};
+  p.kv_dtype = kv_dtype;
+  p.n_h = n_h;
+  p.num_rows = 1;
+  return decode_tc_supported(p) ? MLA_KERNEL_TC_BF16 : MLA_KERNEL_SIMT_F32;
+}
+
 int mla_num_splits(int B, int max_seq_len, int n_h) {
   if (B < 1 || max_seq_len < 0 || !valid_heads(n_h)) return 1;
   const int tiles = ceil_div(max_seq_len, kPage);

@@ -3,7 +3,10 @@ run the library, and evaluate the oracle on chosen (sequence, head) samples."""
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
+
 import workloads as W
 from oracle import fp8_e4m3, mla_oracle
 
@@ -66,5 +69,9 @@ def tol_stats(got: np.ndarray, ref: np.ndarray) -> tuple[float, float]:
 
 def assert_within_tolerance(got, ref, what=""):
     mx, mn = tol_stats(got, ref)
+    log = os.environ.get("MLA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(f"{os.environ.get('PYTEST_CURRENT_TEST', '?').split(' ')[0]}\t{what}\tmax_rel={mx:.3e}\tmean_rel={mn:.3e}\n")
     assert mx <= MAX_REL and mn <= MEAN_REL, f"{what}: max_rel={mx:.3e} mean_rel={mn:.3e}"
     return mx, mn

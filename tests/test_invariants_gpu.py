@@ -56,11 +56,13 @@ def test_zero_query_gives_latent_mean(cuda_device, name):
 
 
 def test_split_count_invariance(cuda_device):
+    # Different split counts round P (bf16) against different running maxima, so the
+    # results agree to the parity tolerance, not bit for bit.
     case = Case(W.WORKLOADS["v2_b32_l4096"], cuda_device)
-    ref = case.run(n_splits=1)["o"].clone()
+    ref = case.run(n_splits=1)["o"].double().cpu().numpy()
     for S in (2, 5, 64, 0):
-        o = case.run(n_splits=S)["o"]
-        torch.testing.assert_close(o, ref, rtol=2e-5, atol=2e-6)
+        o = case.run(n_splits=S)["o"].double().cpu().numpy()
+        assert_within_tolerance(o, ref, f"S={S} vs S=1")
 
 
 def test_paged_equals_contiguous_and_permutation_invariance(cuda_device):
