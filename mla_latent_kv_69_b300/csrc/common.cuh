@@ -7,7 +7,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
-#include "../../include/mla.h"
+#include "mla.h"
 
 namespace mla {
 
