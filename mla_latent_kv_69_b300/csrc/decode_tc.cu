@@ -2,28 +2,32 @@
 //
 // With W_UK folded into the query and W_UV applied after the latent-space sum
 // ("DeepSeek-V2 机制拆解" (discosf.com), §长上下文推理的第一瓶颈), all n_h heads of one
-// sequence attend over the same 576-wide cache rows, so per 64-token tile the work is
-// two dense contractions with the heads as the M dimension:
-//     S[128 x 64]  = Q[128 x 576] · C[64 x 576]^T        (scores, fp32 in TMEM)
-//     O[128 x 512] += P[128 x 64] · C[64 x 0:512]        (latent output, fp32 in TMEM)
-// O alone fills the 512 TMEM columns of an SM, so one work unit (sequence b, split s)
-// runs on a cluster of two CTAs on two SMs:
-//   CTA0  Q (bf16) lives in TMEM columns 0..287 and S in two 64-column buffers; it
-//         issues S = Q·C^T with the A operand read from TMEM, runs the online softmax
-//         (one thread per head, exp2 with a running maximum that is only raised when a
-//         tile's maximum exceeds it by 2^8), and stores P (bf16) straight into CTA1's
-//         shared memory over DSMEM.
-//   CTA1  owns the 128 x 512 fp32 O accumulator (all of its TMEM) and issues O += P·V,
-//         V being the same cache tile read as an MN-major operand. Its four row warps
-//         rescale O rows when CTA0 raised a maximum, zero the unused rows of a ragged
-//         last tile, and write the normalised o_part / lse_part at the end.
-// Each cache tile is fetched from HBM once: the eight 8 KB boxes of c_KV (dims 0..511)
-// are TMA-multicast into both CTAs (four issued by each), and the RoPE-key box (dims
-// 512..575) goes to CTA0 only. A 3-stage ring of mbarriers paces the loads; a stage is
-// refilled once both CTAs' tensor-core work on it has committed.
+// sequence attend over the same 576-wide cache rows, so every tile of tokens is two
+// dense contractions with the heads as the M dimension:
+//     S[128 x 128] = Q[128 x 576] · C[128 x 576]^T       (scores, fp32 in TMEM)
+//     O[128 x 512] += P[128 x 128] · C[128 x 0:512]      (latent output, fp32 in TMEM)
+// O alone fills the 512 TMEM columns of an SM, so a work unit (sequence b, split s)
+// runs on a cluster of two CTAs that exchange only P:
+//   score CTA (rank 0)  Q (bf16) in TMEM columns 0..287, S in columns 288..415.
+//       For each 128-token tile it streams the nine 64-dim column slices of the rows
+//       (16 KB each) through an 11-slot ring, issues S = Q·C^T as 36 MMAs of N = 128,
+//       and runs the online softmax on eight warps (two threads per head, 64 tokens
+//       each). P (bf16) is written to a local staging panel and bulk-copied to the
+//       value CTA, one 64-token panel at a time.
+//   value CTA (rank 1)  owns the 128 x 512 fp32 O accumulator (all of its TMEM).
+//       It reads the c_KV part of the same rows itself (an L2 hit shortly after the
+//       score CTA's read; each cache byte comes from HBM once) into a 3-stage ring and
+//       issues O += P·V per 64-token step as 8 MMAs of N = 256, V being the cache
+//       rows read as an MN-major operand.
+// A tensor-core instruction costs at least ~64 cycles whatever N <= 128, so the score
+// side uses N = 128 token tiles; the shared-memory link between the two SMs is narrow
+// (~20 B/clk), so only P (16 KB per 64 tokens) crosses it, never fp32 scores.
 //
-// Every wait is bounded (2 s); on expiry the CTA records MLA_ERR_TIMEOUT in the status
-// word, tells the peer to stop, drains its own loads and MMAs, frees TMEM and returns.
+// The running maximum of each head is only raised when a tile exceeds it by 2^8; the
+// rare raise is voted across the softmax warps and O rows are rescaled by the value
+// CTA before the tile's PV. Every wait is bounded (2 s); on expiry the CTA records
+// MLA_ERR_TIMEOUT in the status word, tells the peer to stop, drains its own copies
+// and tensor-core work, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -39,78 +43,99 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTile = 64;                 // tokens per tile (= one page)
-constexpr int kStages = 3;
-constexpr int kBox = 64 * 64 * 2;         // one TMA box: 64 rows x 64 bf16 (128 B rows, 128B swizzle)
-constexpr int kCStage = 8 * kBox;         // c_KV part of a tile: dims 0..511
-constexpr int kPBytes = 128 * 64 * 2;     // P tile: 128 heads x 64 tokens bf16
-constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 row warps
+constexpr int kTile = 128;                 // tokens per score tile (the N of S = Q·C^T)
+constexpr int kHalf = 64;                  // tokens per value step (= one page)
+constexpr int kBox = 64 * 128;             // one TMA box: 64 rows x 64 bf16 (128 B rows, 128B swizzle)
+constexpr int kSlice = 2 * kBox;           // score ring slot: 128 rows x 64 dims
+constexpr int kRing = 11;
+constexpr int kCStages = 3;
+constexpr int kCStage = 8 * kBox;          // value stage: 64 rows x 512 dims
+constexpr int kPanel = 128 * 128;          // P for 64 tokens: 128 heads x 64 bf16
+constexpr int kMsg = kPanel + 512 + 16;    // panel, 128 fp32 rescale factors, flag word
+constexpr int kMsgSlot = kPanel + 1024;    // keeps panels 1024-byte aligned
+constexpr int kFinBytes = 128 * 2 * 4;     // final (m, l) per head
+constexpr int kThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2..9 row warps
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr float kRescaleLog2 = 8.f;       // raise the running max only when a tile exceeds it by 2^8
+constexpr float kRescaleLog2 = 8.f;
 
-constexpr uint32_t kQCol = 0;             // CTA0 TMEM: Q as bf16 pairs (288 columns)
-constexpr uint32_t kSCol = 288;           // CTA0 TMEM: S buffers, 2 x 64 columns
-constexpr uint32_t kOCol = 0;             // CTA1 TMEM: O, 512 columns
+constexpr uint32_t kQCol = 0;              // score CTA TMEM: Q as bf16 pairs (288 columns)
+constexpr uint32_t kSCol = 288;            // score CTA TMEM: S (128 columns)
+constexpr uint32_t kOCol = 0;              // value CTA TMEM: O (512 columns)
 
-// Shared memory map (offsets from the 1024-byte aligned dynamic base; same in both CTAs,
-// which multicast requires).
-constexpr int OFF_C = 0;                                // [3][64 KB] c_KV boxes 0..7
-constexpr int OFF_X = kStages * kCStage;                // CTA0: [3][8 KB] RoPE-key box; CTA1: [2][16 KB] P
-constexpr int OFF_FACT = OFF_X + 2 * kPBytes;           // CTA1: [2][128] fp32 rescale factors
-constexpr int OFF_FLAGS = OFF_FACT + 2 * 128 * 4;       // CTA1: [2][4] int "some row of this quarter rescales"
-constexpr int OFF_ML = OFF_FLAGS + 64;                  // CTA1: [128][2] fp32 final (max, sum) per head
-constexpr int OFF_BAR = OFF_ML + 128 * 2 * 4;
+// Shared memory (offsets from the 1024-byte aligned dynamic base).
+//   score CTA
+constexpr int S_RING = 0;                              // kRing x 16 KB (Q is staged in slots 0..8 first)
+constexpr int S_STAGE = S_RING + kRing * kSlice;       // 2 x kMsgSlot: P panels + header, send side
+constexpr int S_MX = S_STAGE + 2 * kMsgSlot;           // [2 tiles][2 halves][128] fp32 maxima, then l halves
+constexpr int S_FIN = S_MX + 2 * 2 * 128 * 4;          // final (m, l) per head
+constexpr int S_END = S_FIN + kFinBytes;
+//   value CTA
+constexpr int V_CST = 0;                               // kCStages x 64 KB
+constexpr int V_MSG = V_CST + kCStages * kCStage;      // 2 x kMsgSlot receive side; the final (m, l) lands in slot 0
+constexpr int V_END = V_MSG + 2 * kMsgSlot;
+//   both (same offset in both CTAs: remote arrivals and copies address it by offset)
+constexpr int OFF_BAR = (S_END > V_END ? S_END : V_END);
 enum Bar {
-  B_FULL = 0,                // [3] tile landed (TMA transaction bytes)
-  B_EMPTY = B_FULL + 3,      // [3] both CTAs' MMAs finished with the stage (2 arrivals)
-  B_SFULL = B_EMPTY + 3,     // [2] CTA0: S buffer written by QK^T
-  B_SFREE = B_SFULL + 2,     // [2] CTA0: S buffer read by the softmax threads (128)
-  B_QREADY = B_SFREE + 2,    // CTA0: Q stored into TMEM (128)
-  B_PFULL = B_QREADY + 1,    // [2] CTA1: P, factors and flags written by CTA0 (128 remote)
-  B_PFREE = B_PFULL + 2,     // [2] CTA0: CTA1's PV MMA finished reading a P buffer (1 remote commit)
-  B_FLUSH = B_PFREE + 2,     // MMA warp: all previously issued MMAs completed
-  B_CREQ = B_FLUSH + 1,      // CTA1: command for the row warps (1)
-  B_CDONE = B_CREQ + 1,      // CTA1: row warps finished the command (128)
-  B_MLREADY = B_CDONE + 1,   // CTA1: final (max, sum) received (128 remote)
-  B_COUNT = B_MLREADY + 1
+  SB_SLOT_FULL = 0,                       // [kRing] score: slice landed
+  SB_SLOT_EMPTY = SB_SLOT_FULL + kRing,   // [kRing] score: QK MMAs done with the slice
+  SB_QFULL = SB_SLOT_EMPTY + kRing,       // score: Q landed in slots 0..8
+  SB_QREADY = SB_QFULL + 1,               // score: Q copied into TMEM (256)
+  SB_SFULL = SB_QREADY + 1,               // score: S written
+  SB_SFREE = SB_SFULL + 1,                // score: S read by the softmax threads (256)
+  SB_PFREE = SB_SFREE + 1,                // [2] score: the value CTA's PV finished with panel j (remote commit)
+  SB_FLUSH = SB_PFREE + 2,                // score MMA warp: all MMAs done
+  VB_CFULL = SB_FLUSH + 1,                // [kCStages] value: stage landed
+  VB_CEMPTY = VB_CFULL + kCStages,        // [kCStages] value: PV done with the stage
+  VB_PFULL = VB_CEMPTY + kCStages,        // [2] value: P panel j received (bulk copy bytes)
+  VB_FIN = VB_PFULL + 2,                  // value: final (m, l) received
+  VB_FLUSH = VB_FIN + 1,                  // value MMA warp: all MMAs done
+  VB_CREQ = VB_FLUSH + 1,                 // value: command for the row warps (1)
+  VB_CDONE = VB_CREQ + 1,                 // value: row warps finished it (256)
+  B_COUNT = VB_CDONE + 1
 };
-constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;         // tmem base, abort flag, command word
+constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;   // tmem base, abort flag, command word, O-initialised flag
 constexpr int kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(S_STAGE % 1024 == 0 && V_MSG % 1024 == 0 && kMsgSlot % 1024 == 0, "panel alignment");
 
 enum Cmd { CMD_ZERO = 1, CMD_RESCALE = 2, CMD_DONE = 4 };
 
-struct TileInfo {
-  int row0;     // first cache row of the tile (the TMA y coordinate)
-  int nvalid;   // tokens of the tile that belong to the split
-  bool valid;   // the tile's rows lie inside the caller's buffers
+// 64-token half u of the split [st, en) of sequence b.
+struct HalfInfo {
+  int row0;     // first cache row (the TMA y coordinate)
+  int nvalid;   // tokens of the half that belong to the split
+  bool load;    // some token is valid and its rows lie inside the caller's buffers
 };
 
-__device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int t0, int en) {
-  TileInfo ti;
-  ti.nvalid = min(kTile, en - t0);
-  ti.valid = true;
-  ti.row0 = 0;
+__device__ __forceinline__ HalfInfo half_info(const DecodeParams& p, int b, int st, int en, int u, bool record) {
+  HalfInfo hi;
+  const int t0 = st + kHalf * u;
+  hi.nvalid = max(0, min(kHalf, en - t0));
+  hi.row0 = 0;
+  hi.load = hi.nvalid > 0;
+  if (!hi.load) return hi;
+  bool valid = true;
   if (p.block_table) {
     const int pi = t0 >> 6;
     const int page = pi < p.max_pages ? p.block_table[(int64_t)b * p.max_pages + pi] : -1;
-    if (page < 0 || (int64_t)page * kTile >= p.num_rows) ti.valid = false;
-    else ti.row0 = page * kTile;
+    if (page < 0 || (int64_t)page * kHalf >= p.num_rows) valid = false;
+    else hi.row0 = page * kHalf;
   } else {
     const int64_t row = (int64_t)b * p.seq_stride + t0;
     if (t0 >= p.seq_stride || row >= p.num_rows) {
-      ti.valid = false;
+      valid = false;
     } else {
-      ti.row0 = (int)row;
+      hi.row0 = (int)row;
       const int64_t room = (p.seq_stride - t0) < (p.num_rows - row) ? (p.seq_stride - t0) : (p.num_rows - row);
-      if (room < ti.nvalid) ti.nvalid = (int)room;
+      if (room < hi.nvalid) hi.nvalid = (int)room;
     }
   }
-  if (!ti.valid) {
-    ti.nvalid = 0;
-    ti.row0 = (int)(p.num_rows < (int64_t)(INT_MAX - kTile) ? p.num_rows : (int64_t)(INT_MAX - kTile));  // out of range: TMA fills zeros
+  if (!valid) {
+    if (record) record_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+    hi.nvalid = 0;
+    hi.load = false;
   }
-  return ti;
+  return hi;
 }
 
 // A bounded wait taken by all 32 lanes of a warp together: every lane returns the same
@@ -128,8 +153,18 @@ __device__ __forceinline__ void give_up(const DecodeParams& p, volatile int* abo
   st_cluster_u32(mapa(smem_u32(smem + OFF_MISC + 4), peer), 1u);
 }
 
+// Slot and use index of score slice k (tile k / 9, column box k % 9). Q occupies slots
+// 0..8 before the first cache slice, so slice k goes to slot (9 + k) % kRing and that
+// slot has held (9 + k) / kRing - [slot < 9] cache slices before it.
+__device__ __forceinline__ int slice_slot(int k) { return (9 + k) % kRing; }
+__device__ __forceinline__ int slice_prior_uses(int k) {
+  const int r = slice_slot(k);
+  return (9 + k) / kRing - (r < 9 ? 1 : 0);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap, float scale_log2) {
+decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
+                 const __grid_constant__ CUtensorMap qmap, float scale_log2) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
@@ -140,6 +175,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
   int st, en;
   split_range(L, p.S, s, &st, &en);
   const int n_tiles = (en - st + kTile - 1) / kTile;
+  const int n_halves = 2 * n_tiles;
 
   if (n_tiles == 0) {   // empty split: nothing crosses the cluster
     if (rank == 1) {
@@ -151,7 +187,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
     }
     return;
   }
-  if (smem_u32(smem) & 1023u) {   // the 128B swizzle needs 1024-byte aligned stages
+  if (smem_u32(smem) & 1023u) {   // the 128B swizzle needs 1024-byte aligned slots (same in both CTAs)
     if (threadIdx.x == 0) record_status(p.status, MLA_ERR_UNSUPPORTED);
     return;
   }
@@ -160,24 +196,37 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   volatile int* cmd_word = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
+  volatile int* o_init_word = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int k = 0; k < kStages; ++k) {
-      mbar_init(&bars[B_FULL + k], 1);
-      mbar_init(&bars[B_EMPTY + k], 2);
+    *o_init_word = 0;
+    for (int k = 0; k < kRing; ++k) {
+      mbar_init(&bars[SB_SLOT_FULL + k], 1);
+      mbar_init(&bars[SB_SLOT_EMPTY + k], 1);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars[B_SFULL + k], 1);
-      mbar_init(&bars[B_SFREE + k], 128);
-      mbar_init(&bars[B_PFULL + k], 128);
-      mbar_init(&bars[B_PFREE + k], 1);
+    mbar_init(&bars[SB_QFULL], 1);
+    mbar_init(&bars[SB_QREADY], 256);
+    mbar_init(&bars[SB_SFULL], 1);
+    mbar_init(&bars[SB_SFREE], 256);
+    mbar_init(&bars[SB_PFREE], 1);
+    mbar_init(&bars[SB_PFREE + 1], 1);
+    mbar_init(&bars[SB_FLUSH], 1);
+    for (int k = 0; k < kCStages; ++k) {
+      mbar_init(&bars[VB_CFULL + k], 1);
+      mbar_init(&bars[VB_CEMPTY + k], 1);
     }
-    mbar_init(&bars[B_QREADY], 128);
-    mbar_init(&bars[B_FLUSH], 1);
-    mbar_init(&bars[B_CREQ], 1);
-    mbar_init(&bars[B_CDONE], 128);
-    mbar_init(&bars[B_MLREADY], 128);
+    mbar_init(&bars[VB_PFULL], 1);
+    mbar_init(&bars[VB_PFULL + 1], 1);
+    mbar_init(&bars[VB_FIN], 1);
+    mbar_init(&bars[VB_FLUSH], 1);
+    mbar_init(&bars[VB_CREQ], 1);
+    mbar_init(&bars[VB_CDONE], 256);
+    if (rank == 1) {   // the first tile's P panels and the final message may arrive any time after the cluster sync
+      mbar_arrive_expect_tx(&bars[VB_PFULL], kMsg);
+      mbar_arrive_expect_tx(&bars[VB_PFULL + 1], kMsg);
+      mbar_arrive_expect_tx(&bars[VB_FIN], kFinBytes);
+    }
     fence_mbar_init_cluster();
   }
   if (warp == 1) {
@@ -186,220 +235,312 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // the peer's barriers exist before any multicast or remote arrive
+  cluster_sync();   // the peer's barriers exist before any remote arrival or copy
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------------
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      prefetch_tmap(&tmap);
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int stg = i % kStages;
-        if (i >= kStages && !mbar_wait<true>(&bars[B_EMPTY + stg], ((i / kStages) - 1) & 1, abort_flag, kWaitNs)) {
-          give_up(p, abort_flag, smem, peer);
-          break;
+  if (rank == 0) {
+    // =============================== score CTA =========================================
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---- TMA producer: Q, then the column slices of every tile ----
+        const uint64_t pol_first = l2_policy_evict_first();
+        const uint64_t pol_last = l2_policy_evict_last();   // c_KV is read again by the value CTA
+        prefetch_tmap(&cmap);
+        prefetch_tmap(&qmap);
+        const int qrows = p.n_h < 128 ? p.n_h : 128;
+        mbar_arrive_expect_tx(&bars[SB_QFULL], 9 * qrows * 128);
+        for (int c = 0; c < 9; ++c)
+          tma_load_2d(smem + S_RING + c * kSlice, &qmap, &bars[SB_QFULL], 64 * c, b * p.n_h, pol_first);
+        int issued = 0;
+        HalfInfo h0{}, h1{};
+        for (int k = 0; k < 9 * n_tiles; ++k) {
+          const int i = k / 9, c = k % 9;
+          const int r = slice_slot(k), prior = slice_prior_uses(k);
+          bool ok = true;
+          if (r < 9 && prior == 0) ok = mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs);
+          if (ok && prior > 0) ok = mbar_wait(&bars[SB_SLOT_EMPTY + r], (prior - 1) & 1, abort_flag, kWaitNs);
+          if (!ok) {
+            give_up(p, abort_flag, smem, peer);
+            break;
+          }
+          if (c == 0) {
+            h0 = half_info(p, b, st, en, 2 * i, true);
+            h1 = half_info(p, b, st, en, 2 * i + 1, true);
+          }
+          const uint32_t bytes = (h0.load ? kBox : 0) + (h1.load ? kBox : 0);
+          unsigned char* dst = smem + S_RING + r * kSlice;
+          const uint64_t pol = c < 8 ? pol_last : pol_first;
+          if (bytes) {
+            mbar_arrive_expect_tx(&bars[SB_SLOT_FULL + r], bytes);
+            if (h0.load) tma_load_2d(dst, &cmap, &bars[SB_SLOT_FULL + r], 64 * c, h0.row0, pol);
+            if (h1.load) tma_load_2d(dst + kBox, &cmap, &bars[SB_SLOT_FULL + r], 64 * c, h1.row0, pol);
+          } else {
+            mbar_arrive(&bars[SB_SLOT_FULL + r]);
+          }
+          issued = k + 1;
         }
-        const TileInfo ti = tile_info(p, b, st + i * kTile, en);
-        if (!ti.valid && rank == 0) record_status(p.status, MLA_ERR_DEVICE_BOUNDS);
-        unsigned char* cst = smem + OFF_C + stg * kCStage;
-        if (rank == 0) {
-          mbar_arrive_expect_tx(&bars[B_FULL + stg], kCStage + kBox);
-          for (int j = 0; j < 4; ++j) tma_load_2d_mc(cst + j * kBox, &tmap, &bars[B_FULL + stg], 64 * j, ti.row0, 0x3, pol);
-          tma_load_2d(smem + OFF_X + stg * kBox, &tmap, &bars[B_FULL + stg], 512, ti.row0, pol);
-        } else {
-          mbar_arrive_expect_tx(&bars[B_FULL + stg], kCStage);
-          for (int j = 4; j < 8; ++j) tma_load_2d_mc(cst + j * kBox, &tmap, &bars[B_FULL + stg], 64 * j, ti.row0, 0x3, pol);
-        }
-        issued = i + 1;
-      }
-      // Loads still in flight land before the CTA may leave.
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        // Loads still in flight land before the CTA may leave.
         const volatile int never = 0;
-        mbar_wait<true>(&bars[B_FULL + i % kStages], (i / kStages) & 1, &never, kWaitNs / 4);
+        mbar_wait(&bars[SB_QFULL], 0, &never, kWaitNs / 4);
+        for (int k = max(0, issued - kRing); k < issued; ++k)
+          mbar_wait(&bars[SB_SLOT_FULL + slice_slot(k)], slice_prior_uses(k) & 1, &never, kWaitNs / 4);
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      if (rank == 0) {
-        // ---------------------------- S = Q · C^T -----------------------------------
-        const uint32_t idq = idesc_f16(128, 64, false, false, false);
-        bool ok = mbar_wait(&bars[B_QREADY], 0, abort_flag, kWaitNs);
-        tc_fence_after();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---- S = Q · C^T, 36 MMAs of 128 x 128 x 16 per tile ----
+        const uint32_t idq = idesc_f16(128, kTile, false, false, false);
+        bool ok = mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs);
         for (int i = 0; ok && i < n_tiles; ++i) {
-          const int stg = i % kStages, sb = i & 1;
-          if (!mbar_wait<true>(&bars[B_FULL + stg], (i / kStages) & 1, abort_flag, kWaitNs) ||
-              (i >= 2 && !mbar_wait(&bars[B_SFREE + sb], ((i >> 1) - 1) & 1, abort_flag, kWaitNs))) {
+          if (i > 0 && !mbar_wait(&bars[SB_SFREE], (i - 1) & 1, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t cb = smem_u32(smem + OFF_C + stg * kCStage);
-          const uint32_t kb = smem_u32(smem + OFF_X + stg * kBox);
-          const uint32_t d = tmem + kSCol + 64 * sb;
+          for (int c = 0; c < 9; ++c) {
+            const int k = 9 * i + c, r = slice_slot(k);
+            if (!mbar_wait(&bars[SB_SLOT_FULL + r], slice_prior_uses(k) & 1, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t base = smem_u32(smem + S_RING + r * kSlice);
 #pragma unroll
-          for (int k = 0; k < kRow / 16; ++k) {
-            const int box = k >> 2;
-            const uint32_t addr = (box < 8 ? cb + box * kBox : kb) + (k & 3) * 32;
-            mma_ts(d, tmem + kQCol + 8 * k, sdesc_sw128(addr, 16, 1024), idq, k > 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + kSCol, tmem + kQCol + 8 * (4 * c + kk), sdesc_sw128(base + 32 * kk, 16, 1024), idq,
+                     (c | kk) ? 1u : 0u);
+            mma_commit(&bars[SB_SLOT_EMPTY + r]);
           }
-          mma_commit(&bars[B_SFULL + sb]);
-          mma_commit_mc(&bars[B_EMPTY + stg], 0x3);
+          if (!ok) break;
+          mma_commit(&bars[SB_SFULL]);
         }
         if (!ok) give_up(p, abort_flag, smem, peer);
-        mma_commit(&bars[B_FLUSH]);
+        mma_commit(&bars[SB_FLUSH]);
         const volatile int never = 0;
-        mbar_wait(&bars[B_FLUSH], 0, &never, kWaitNs);
-      } else {
-        // ---------------------------- O += P · V -------------------------------------
-        const uint32_t idv = idesc_f16(128, 256, false, false, true);
-        int ncmd = 0, nflush = 0;
-        bool ok = true;
-        const volatile int never = 0;
-        for (int i = 0; i < n_tiles; ++i) {
-          const int stg = i % kStages, sb = i & 1;
-          if (!mbar_wait<true>(&bars[B_FULL + stg], (i / kStages) & 1, abort_flag, kWaitNs) ||
-              !mbar_wait<true>(&bars[B_PFULL + sb], (i >> 1) & 1, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
-          }
-          const TileInfo ti = tile_info(p, b, st + i * kTile, en);
-          const volatile int* fl = reinterpret_cast<const volatile int*>(smem + OFF_FLAGS) + sb * 4;
-          int c = 0;
-          if (ti.nvalid < kTile) c |= CMD_ZERO;
-          if (fl[0] | fl[1] | fl[2] | fl[3]) c |= CMD_RESCALE;
-          if (c) {
-            if (c & CMD_RESCALE) {   // O must be quiescent before its rows are rescaled
-              mma_commit(&bars[B_FLUSH]);
-              if (!mbar_wait(&bars[B_FLUSH], nflush & 1, &never, kWaitNs)) { ok = false; break; }
-              ++nflush;
-            }
-            *cmd_word = (i << 8) | c;
-            mbar_arrive(&bars[B_CREQ]);
-            if (!mbar_wait(&bars[B_CDONE], ncmd & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            ++ncmd;
-          }
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t pb = smem_u32(smem + OFF_X + sb * kPBytes);
-          const uint32_t vb = smem_u32(smem + OFF_C + stg * kCStage);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(pb + 32 * kk, 16, 1024);
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-              const uint64_t bd = sdesc_sw128(vb + 4 * nh * kBox + kk * 2048, kBox, 1024);
-              mma_ss(tmem + kOCol + 256 * nh, a, bd, idv, (i > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          mma_commit_mc(&bars[B_EMPTY + stg], 0x3);
-          mma_commit_mc(&bars[B_PFREE + sb], 0x1);
-        }
-        if (!ok) give_up(p, abort_flag, smem, peer);
-        mma_commit(&bars[B_FLUSH]);                  // O final before the epilogue reads it
-        mbar_wait(&bars[B_FLUSH], nflush & 1, &never, kWaitNs);
-        *cmd_word = CMD_DONE;
-        mbar_arrive(&bars[B_CREQ]);
+        mbar_wait(&bars[SB_FLUSH], 0, &never, kWaitNs);
       }
-    }
-  } else {
-    // ------------------------------ row warps (2..5) ---------------------------------
-    const int q = warp & 3;                       // TMEM lane quarter this warp may access
-    const int h = q * 32 + lane;                  // head (= TMEM lane) owned by this thread
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    if (rank == 0) {
-      // Q row h → TMEM (packed bf16 pairs; padded heads are zero)
-      {
-        const uint4* qrow = reinterpret_cast<const uint4*>(p.q_lat + ((int64_t)b * p.n_h + min(h, p.n_h - 1)) * kRow);
-        uint32_t r[32];
+    } else {
+      // ---- softmax: thread (h, j) owns head h, tokens [64 j, 64 j + 64) of each tile ----
+      const int q = warp & 3;
+      const int h = q * 32 + lane;
+      const int j = (warp - 2) >> 2;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      // Q rows → TMEM (packed bf16 pairs; heads beyond n_h are zero)
+      if (warp_wait(&bars[SB_QFULL], 0, abort_flag)) {
 #pragma unroll 1
-        for (int c = 0; c < 9; ++c) {
+        for (int c = j; c < 9; c += 2) {
+          uint32_t r[32];
+          const unsigned char* row = smem + S_RING + c * kSlice + h * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 v = h < p.n_h ? __ldg(qrow + c * 8 + j) : make_uint4(0, 0, 0, 0);
-            r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
+          for (int x = 0; x < 8; ++x) {
+            const uint4 v = h < p.n_h ? *reinterpret_cast<const uint4*>(row + ((x ^ (h & 7)) << 4))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+            r[4 * x] = v.x; r[4 * x + 1] = v.y; r[4 * x + 2] = v.z; r[4 * x + 3] = v.w;
           }
           MLA_TMEM_ST32(trow + kQCol + 32 * c, r);
         }
         tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars[B_QREADY]);
+      } else {
+        give_up(p, abort_flag, smem, peer);
       }
-      // online softmax
+      tc_fence_before();
+      mbar_arrive(&bars[SB_QREADY]);
+
       float m_run = -INFINITY, l_run = 0.f;
-      const uint32_t p_remote = mapa(smem_u32(smem + OFF_X), 1);
-      const uint32_t fact_remote = mapa(smem_u32(smem + OFF_FACT), 1);
-      const uint32_t flags_remote = mapa(smem_u32(smem + OFF_FLAGS), 1);
+      float* mx = reinterpret_cast<float*>(smem + S_MX);
+      const uint32_t msg_remote = mapa(smem_u32(smem + V_MSG + j * kMsgSlot), 1);
+      const uint32_t pfull_remote = mapa(smem_u32(&bars[VB_PFULL + j]), 1);
+      // Every thread runs every iteration and every named barrier; after an abort the
+      // waits return at once and the tiles are processed as fully masked.
       for (int i = 0; i < n_tiles; ++i) {
-        const int sb = i & 1;
-        if (!warp_wait(&bars[B_SFULL + sb], (i >> 1) & 1, abort_flag)) {
-          give_up(p, abort_flag, smem, peer);
-          break;
-        }
-        tc_fence_after();
         uint32_t sr[64];
-        MLA_TMEM_LD32(trow + kSCol + 64 * sb, sr);
-        MLA_TMEM_LD32(trow + kSCol + 64 * sb + 32, (sr + 32));
-        tmem_wait_ld();
+        const bool got = warp_wait(&bars[SB_SFULL], i & 1, abort_flag);
+        if (got) {
+          tc_fence_after();
+          MLA_TMEM_LD32(trow + kSCol + 64 * j, sr);
+          MLA_TMEM_LD32(trow + kSCol + 64 * j + 32, (sr + 32));
+          tmem_wait_ld();
+        }
         tc_fence_before();
-        mbar_arrive(&bars[B_SFREE + sb]);
-        const int nvalid = tile_info(p, b, st + i * kTile, en).nvalid;
+        mbar_arrive(&bars[SB_SFREE]);
+        const int nv = got ? half_info(p, b, st, en, 2 * i + j, false).nvalid : 0;
         float x[64];
         float mt = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          x[j] = j < nvalid ? __uint_as_float(sr[j]) * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[j]);
+        for (int t = 0; t < 64; ++t) {
+          x[t] = t < nv ? __uint_as_float(sr[t]) * scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[t]);
         }
-        float factor = 1.f;
-        bool need = false;
-        if (m_run == -INFINITY) {
-          m_run = mt;                              // nothing accumulated yet
-        } else if (mt > m_run + kRescaleLog2) {
-          factor = ex2(m_run - mt);
-          l_run *= factor;
-          m_run = mt;
-          need = true;
+        // Raise the running maximum only when the tile exceeds it by 2^8 (rare); the
+        // two threads of a head agree on the new value through shared memory.
+        float fac = 1.f;
+        bool row_rescale = false;
+        const uint32_t nneed = named_popc(1, 256, mt > m_run + kRescaleLog2);
+        if (nneed) {
+          float* mxb = mx + (i & 1) * 256;
+          mxb[j * 128 + h] = mt;
+          named_sync(1, 256);
+          const float mrow = fmaxf(mxb[h], mxb[128 + h]);
+          if (mrow > m_run + kRescaleLog2) {
+            if (m_run != -INFINITY) {
+              fac = ex2(m_run - mrow);
+              row_rescale = true;
+            }
+            l_run *= fac;
+            m_run = mrow;
+          }
         }
+        const uint32_t nres = nneed ? named_popc(1, 256, row_rescale) : 0u;
         const bool live = m_run != -INFINITY;
         uint32_t pk[32];
         float lsum = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = live ? ex2(x[2 * j] - m_run) : 0.f;
-          const float p1 = live ? ex2(x[2 * j + 1] - m_run) : 0.f;
+        for (int t = 0; t < 32; ++t) {
+          const float p0 = live ? ex2(x[2 * t] - m_run) : 0.f;
+          const float p1 = live ? ex2(x[2 * t + 1] - m_run) : 0.f;
           const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
           const float2 back = __bfloat1622float2(v);
           lsum += back.x + back.y;                 // the sum of exactly the weights the MMA uses
-          pk[j] = *reinterpret_cast<const uint32_t*>(&v);
+          pk[t] = *reinterpret_cast<const uint32_t*>(&v);
         }
         l_run += lsum;
-        if (i >= 2 && !warp_wait<true>(&bars[B_PFREE + sb], ((i >> 1) - 1) & 1, abort_flag)) {
-          give_up(p, abort_flag, smem, peer);
-          break;
-        }
-        const uint32_t prow = p_remote + sb * kPBytes + h * 128;
+        // The staging panel is free once the value CTA's PV on the previous tile has read it.
+        if (i > 0) mbar_wait<true>(&bars[SB_PFREE + j], (i - 1) & 1, abort_flag, kWaitNs);
+        unsigned char* stg = smem + S_STAGE + j * kMsgSlot;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          st_cluster_v4(prow + ((c ^ (h & 7)) << 4), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-        st_cluster_f32(fact_remote + (sb * 128 + h) * 4, factor);
-        const unsigned any = __ballot_sync(0xffffffffu, need);
-        if (lane == 0) st_cluster_u32(flags_remote + (sb * 4 + q) * 4, any != 0u);
-        fence_proxy_async_cluster();
-        mbar_arrive_remote(&bars[B_PFULL + sb], 1);
+          *reinterpret_cast<uint4*>(stg + h * 128 + ((c ^ (h & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (j == 0) {
+          reinterpret_cast<float*>(stg + kPanel)[h] = fac;
+          if (h == 0) reinterpret_cast<uint32_t*>(stg + kPanel + 512)[0] = nres;
+        }
+        fence_proxy_async_smem();
+        named_sync(2 + j, 128);
+        if (q == 0 && lane == 0 && !*abort_flag) bulk_copy_to_peer(msg_remote, stg, kMsg, pfull_remote);
       }
-      const uint32_t ml_remote = mapa(smem_u32(smem + OFF_ML), 1);
-      st_cluster_f32(ml_remote + h * 8, m_run);
-      st_cluster_f32(ml_remote + h * 8 + 4, l_run);
-      mbar_arrive_remote(&bars[B_MLREADY], 1);
+      // final (m, l) of each head → the value CTA, once its last PV has read both panels
+      named_sync(1, 256);
+      mx[j * 128 + h] = l_run;
+      named_sync(1, 256);
+      float* fin = reinterpret_cast<float*>(smem + S_FIN);
+      if (j == 0) {
+        fin[2 * h] = m_run;
+        fin[2 * h + 1] = mx[h] + mx[128 + h];
+      }
+      fence_proxy_async_smem();
+      named_sync(1, 256);
+      if (warp == 2 && lane == 0) {
+        bool ok = mbar_wait<true>(&bars[SB_PFREE], (n_tiles - 1) & 1, abort_flag, kWaitNs) &&
+                  mbar_wait<true>(&bars[SB_PFREE + 1], (n_tiles - 1) & 1, abort_flag, kWaitNs);
+        if (ok && !*abort_flag)
+          bulk_copy_to_peer(mapa(smem_u32(smem + V_MSG), 1), fin, kFinBytes, mapa(smem_u32(&bars[VB_FIN]), 1));
+      }
+    }
+  } else {
+    // =============================== value CTA =========================================
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---- TMA producer: c_KV of every 64-token step (evict-first: last reader) ----
+        const uint64_t pol = l2_policy_evict_first();
+        prefetch_tmap(&cmap);
+        int issued = 0;
+        for (int u = 0; u < n_halves; ++u) {
+          const int sg = u % kCStages;
+          if (u >= kCStages &&
+              !mbar_wait(&bars[VB_CEMPTY + sg], ((u / kCStages) - 1) & 1, abort_flag, kWaitNs)) {
+            give_up(p, abort_flag, smem, peer);
+            break;
+          }
+          const HalfInfo hi = half_info(p, b, st, en, u, false);
+          if (hi.load) {
+            mbar_arrive_expect_tx(&bars[VB_CFULL + sg], kCStage);
+            unsigned char* dst = smem + V_CST + sg * kCStage;
+            for (int c = 0; c < 8; ++c)
+              tma_load_2d(dst + c * kBox, &cmap, &bars[VB_CFULL + sg], 64 * c, hi.row0, pol);
+          } else {
+            mbar_arrive(&bars[VB_CFULL + sg]);
+          }
+          issued = u + 1;
+        }
+        const volatile int never = 0;
+        for (int u = max(0, issued - kCStages); u < issued; ++u)
+          mbar_wait(&bars[VB_CFULL + u % kCStages], (u / kCStages) & 1, &never, kWaitNs / 4);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---- O += P · V, 8 MMAs of 128 x 256 x 16 per 64-token step ----
+        const uint32_t idv = idesc_f16(128, 256, false, false, true);
+        int ncmd = 0, nflush = 0;
+        bool ok = true, o_init = false;
+        const volatile int never = 0;
+        for (int u = 0; u < n_halves; ++u) {
+          const int i = u >> 1, j = u & 1, sg = u % kCStages;
+          if (!mbar_wait(&bars[VB_CFULL + sg], (u / kCStages) & 1, abort_flag, kWaitNs) ||
+              !mbar_wait<true>(&bars[VB_PFULL + j], i & 1, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          if (i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[VB_PFULL + j], kMsg);   // next tile's panel j
+          const HalfInfo hi = half_info(p, b, st, en, u, false);
+          const unsigned char* msg = smem + V_MSG + j * kMsgSlot;
+          int c = 0;
+          if (j == 0 && o_init && *reinterpret_cast<const volatile uint32_t*>(msg + kPanel + 512) != 0u)
+            c |= CMD_RESCALE;
+          if (hi.nvalid > 0 && hi.nvalid < kHalf) c |= CMD_ZERO;
+          if (c) {
+            if (c & CMD_RESCALE) {   // O must be quiescent before its rows are rescaled
+              mma_commit(&bars[VB_FLUSH]);
+              if (!mbar_wait(&bars[VB_FLUSH], nflush & 1, &never, kWaitNs)) {
+                ok = false;
+                break;
+              }
+              ++nflush;
+            }
+            *cmd_word = (u << 8) | c;
+            mbar_arrive(&bars[VB_CREQ]);
+            if (!mbar_wait(&bars[VB_CDONE], ncmd & 1, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            ++ncmd;
+          }
+          if (hi.nvalid > 0) {
+            tc_fence_after();
+            const uint32_t pb = smem_u32(msg);
+            const uint32_t vb = smem_u32(smem + V_CST + sg * kCStage);
+#pragma unroll
+            for (int kk = 0; kk < kHalf / 16; ++kk) {
+              const uint64_t a = sdesc_sw128(pb + 32 * kk, 16, 1024);
+#pragma unroll
+              for (int nh = 0; nh < 2; ++nh) {
+                const uint64_t bd = sdesc_sw128(vb + 4 * nh * kBox + kk * 2048, kBox, 1024);
+                mma_ss(tmem + kOCol + 256 * nh, a, bd, idv, (o_init || kk > 0) ? 1u : 0u);
+              }
+            }
+            o_init = true;
+          }
+          mma_commit(&bars[VB_CEMPTY + sg]);
+          mma_commit_mc(&bars[SB_PFREE + j], 0x1);
+        }
+        if (!ok) give_up(p, abort_flag, smem, peer);
+        mma_commit(&bars[VB_FLUSH]);   // O final before the epilogue reads it
+        mbar_wait(&bars[VB_FLUSH], nflush & 1, &never, kWaitNs);
+        *o_init_word = o_init ? 1 : 0;
+        *cmd_word = CMD_DONE;
+        mbar_arrive(&bars[VB_CREQ]);
+      }
     } else {
-      // CTA1: commands from the PV issuer, then the epilogue
+      // ---- row warps: commands from the PV issuer, then the epilogue ----
+      const int q = warp & 3;
+      const int h = q * 32 + lane;
+      const int j = (warp - 2) >> 2;
+      const int tid = threadIdx.x - 64;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
       int k = 0;
       bool ok = true;
       while (true) {
-        if (!warp_wait(&bars[B_CREQ], k & 1, abort_flag)) {
+        if (!warp_wait(&bars[VB_CREQ], k & 1, abort_flag)) {
           ok = false;
           give_up(p, abort_flag, smem, peer);
           break;
@@ -407,62 +548,74 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
         ++k;
         const int c = *cmd_word;
         if (c & CMD_DONE) break;
-        const int i = c >> 8;
-        if (c & CMD_ZERO) {
-          const int nvalid = tile_info(p, b, st + i * kTile, en).nvalid;
-          unsigned char* cst = smem + OFF_C + (i % kStages) * kCStage;
-          const int tid = threadIdx.x - 64;
-          for (int idx = tid; idx < (kTile - nvalid) * 64; idx += 128) {
+        const int u = c >> 8;
+        if (c & CMD_ZERO) {   // rows of a ragged step beyond the split: zero V so that 0·V stays 0
+          const int nvalid = half_info(p, b, st, en, u, false).nvalid;
+          unsigned char* cst = smem + V_CST + (u % kCStages) * kCStage;
+          for (int idx = tid; idx < (kHalf - nvalid) * 64; idx += 256) {
             const int row = nvalid + (idx >> 6), box = (idx >> 3) & 7, chunk = idx & 7;
-            *reinterpret_cast<uint4*>(cst + box * kBox + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(cst + box * kBox + row * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
         }
         if (c & CMD_RESCALE) {
           tc_fence_after();
-          const float f = reinterpret_cast<const float*>(smem + OFF_FACT)[(i & 1) * 128 + h];
+          const float f = reinterpret_cast<const float*>(smem + V_MSG + kPanel)[h];
           if (__any_sync(0xffffffffu, f != 1.f)) {
             uint32_t r[32];
 #pragma unroll 1
-            for (int cc = 0; cc < 16; ++cc) {
-              MLA_TMEM_LD32(trow + kOCol + 32 * cc, r);
+            for (int cc = 0; cc < 8; ++cc) {
+              const uint32_t col = kOCol + 256 * j + 32 * cc;
+              MLA_TMEM_LD32(trow + col, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-              MLA_TMEM_ST32(trow + kOCol + 32 * cc, r);
+              for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
+              MLA_TMEM_ST32(trow + col, r);
             }
             tmem_wait_st();
           }
           tc_fence_before();
         }
-        mbar_arrive(&bars[B_CDONE]);
+        mbar_arrive(&bars[VB_CDONE]);
       }
-      // epilogue: o_part = O / l, lse_part = (m + log2 l) · ln 2
-      if (ok && !warp_wait<true>(&bars[B_MLREADY], 0, abort_flag)) {
-        ok = false;
-        give_up(p, abort_flag, smem, peer);
-      }
+      // epilogue: o_part = O / l, lse_part = (m + log2 l) · ln 2, staged in shared memory
+      // (the c_KV stages are idle now) so that the global stores are coalesced rows
+      const bool fin_ok = ok && warp_wait<true>(&bars[VB_FIN], 0, abort_flag);
       tc_fence_after();
-      const float m = reinterpret_cast<const float*>(smem + OFF_ML)[2 * h];
-      const float l = reinterpret_cast<const float*>(smem + OFF_ML)[2 * h + 1];
-      const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
-      float* orow = p.o_part + (((int64_t)b * p.S + s) * p.n_h + h) * kLatent;
-      uint32_t r[32];
+      const float* fin = reinterpret_cast<const float*>(smem + V_MSG);
+      const float m = fin[2 * h];
+      const float l = fin[2 * h + 1];
+      const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
+      const float inv = good ? 1.f / l : 0.f;
+      unsigned char* stg = smem + V_CST;
+      float* obase = p.o_part + ((int64_t)b * p.S + s) * p.n_h * kLatent;
 #pragma unroll 1
-      for (int cc = 0; cc < 16; ++cc) {
-        MLA_TMEM_LD32(trow + kOCol + 32 * cc, r);
-        tmem_wait_ld();
-        if (h < p.n_h) {
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t r[32];
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          MLA_TMEM_LD32(trow + kOCol + 256 * pass + 128 * j + 32 * cc, r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            reinterpret_cast<float4*>(orow + 32 * cc)[j] =
-                make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
-                            __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+          for (int x = 0; x < 8; ++x) {
+            const int chunk = 32 * j + 8 * cc + x;
+            *reinterpret_cast<float4*>(stg + h * 1024 + ((chunk ^ (h & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
+                            __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
+          }
         }
+        named_sync(1, 256);
+        for (int idx = tid; idx < 128 * 64; idx += 256) {
+          const int row = idx >> 6, ch = idx & 63;
+          if (row < p.n_h)
+            *reinterpret_cast<float4*>(obase + (int64_t)row * kLatent + 256 * pass + 4 * ch) =
+                *reinterpret_cast<const float4*>(stg + row * 1024 + ((ch ^ (row & 7)) << 4));
+        }
+        named_sync(1, 256);
       }
-      if (h < p.n_h)
+      if (j == 0 && h < p.n_h)
         p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] =
-            (ok && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            good ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
       tc_fence_before();
     }
   }
@@ -487,15 +640,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// One 2D map over the whole cache: rows of 576 bf16, boxes of 64 rows x 64 columns.
-bool make_cache_map(const DecodeParams& p, CUtensorMap* map) {
+// 2D map over rows of 576 bf16 with boxes of `box_rows` rows x 64 columns (128B swizzle).
+bool make_row_map(const void* base, int64_t rows, int box_rows, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)p.num_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.data), dims, strides, box, es,
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -508,8 +661,9 @@ bool decode_tc_supported(const DecodeParams& p) {
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_t st) {
   (void)max_seq_len;
-  CUtensorMap map;
-  if (!make_cache_map(p, &map)) return cudaErrorInvalidValue;
+  CUtensorMap cmap, qmap;
+  if (!make_row_map(p.data, p.num_rows, 64, &cmap)) return cudaErrorInvalidValue;
+  if (!make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, &qmap)) return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -518,7 +672,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   if (attr_err != cudaSuccess) return attr_err;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t ctas = 2ll * p.B * p.S;
-  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, map, scale_log2);
+  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, cmap, qmap, scale_log2);
   return cudaGetLastError();
 }
 
@@ -530,9 +684,10 @@ int decode_tc_num_splits(int B, int tiles, int n_h, int sms) {
   for (int S = 1; S <= MLA_MAX_SPLITS && S <= tiles; ++S) {
     const int per = ceil_div(tiles, S);
     const int waves = ceil_div(B * S, pairs);
-    // time in tile units: waves of `per` tiles, plus ~3.6 tile-equivalents of
-    // partial-result traffic per unit (256 KB fp32 written, read back by the merge)
-    const double t = waves * (per + 3.6) + 3.6 * (double)B * S / pairs;
+    // time in 64-token tile units: waves of `per` tiles plus a fixed start/drain cost
+    // per unit (~4 tiles: Q load, pipeline fill, the 256 KB partial-result write), plus
+    // the merge reading the partials back
+    const double t = waves * (per + 4.0) + 2.0 * (double)B * S / pairs;
     if (t < best_t - 1e-9) {
       best_t = t;
       best = S;

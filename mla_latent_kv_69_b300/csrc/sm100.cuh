@@ -278,3 +278,40 @@ __device__ __forceinline__ float ex2(float x) {
 }
 }  // namespace sm100
 }  // namespace mla
+
+namespace mla {
+namespace sm100 {
+// Bulk copy from this CTA's shared memory into a peer CTA's shared memory; the bytes
+// complete on the peer's mbarrier. `dst` and `bar` are shared::cluster addresses (mapa).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Named barrier over `count` threads (a multiple of 32) with id `id` (1..15).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the number of participating threads with v != 0.
+__device__ __forceinline__ uint32_t named_popc(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.popc.u32 %0, %1, %2, p;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)v)
+      : "memory");
+  return r;
+}
+// 32 lanes x 32 bits, 16 columns (half of MLA_TMEM_LD32).
+#define MLA_TMEM_ST16(taddr, r)                                                                         \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+               "%13,%14,%15,%16};" ::"r"(taddr),                                                        \
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),  \
+               "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),        \
+               "r"(r[15])                                                                               \
+               : "memory")
+}  // namespace sm100
+}  // namespace mla
