@@ -10,15 +10,19 @@
 // runs on a cluster of two CTAs that exchange only P:
 //   score CTA (rank 0)  Q (bf16) in TMEM columns 0..287, S in columns 288..415.
 //       For each 128-token tile it streams the nine 64-dim column slices of the rows
-//       (16 KB each) through an 11-slot ring, issues S = Q·C^T as 36 MMAs of N = 128,
-//       and runs the online softmax on eight warps (two threads per head, 64 tokens
-//       each). P (bf16) is written to a local staging panel and bulk-copied to the
-//       value CTA, one 64-token panel at a time.
+//       (16 KB each) through a ring of four 3-slice groups, issues S = Q·C^T as 36 MMAs
+//       of N = 128, and runs the online softmax on eight warps (two threads per head,
+//       64 tokens each). P (bf16) is written to a local staging panel and bulk-copied
+//       to the value CTA, one 64-token panel at a time.
 //   value CTA (rank 1)  owns the 128 x 512 fp32 O accumulator (all of its TMEM).
 //       It reads the c_KV part of the same rows itself (an L2 hit shortly after the
 //       score CTA's read; each cache byte comes from HBM once) into a 3-stage ring and
 //       issues O += P·V per 64-token step as 8 MMAs of N = 256, V being the cache
 //       rows read as an MN-major operand.
+// The TMA engine spends a roughly fixed time per box row, so loads use 3D tensor maps
+// (64 columns x rows x column chunks) that fetch several 128-byte chunks of each row
+// per instruction; the shared-memory image is the same chunk-major 128B-swizzled
+// layout as one 2D box per chunk.
 // A tensor-core instruction costs at least ~64 cycles whatever N <= 128, so the score
 // side uses N = 128 token tiles; the shared-memory link between the two SMs is narrow
 // (~20 B/clk), so only P (16 KB per 64 tokens) crosses it, never fp32 scores.
@@ -46,13 +50,13 @@ using namespace sm100;
 constexpr int kTile = 128;                 // tokens per score tile (the N of S = Q·C^T)
 constexpr int kHalf = 64;                  // tokens per value step (= one page)
 constexpr int kBox = 64 * 128;             // one TMA box: 64 rows x 64 bf16 (128 B rows, 128B swizzle)
-constexpr int kSlice = 2 * kBox;           // score ring slot: 128 rows x 64 dims
-constexpr int kRing = 11;
+constexpr int kSlice = 2 * kBox;           // one column slice of a score tile: 128 rows x 64 dims
+constexpr int kGroup = 3 * kSlice;         // score ring slot: three slices (one TMA instruction)
+constexpr int kRing = 4;
 constexpr int kCStages = 3;
 constexpr int kCStage = 8 * kBox;          // value stage: 64 rows x 512 dims
 constexpr int kPanel = 128 * 128;          // P for 64 tokens: 128 heads x 64 bf16
-constexpr int kMsg = kPanel + 512 + 16;    // panel, 128 fp32 rescale factors, flag word
-constexpr int kMsgSlot = kPanel + 1024;    // keeps panels 1024-byte aligned
+constexpr int kHdr = 512 + 16;             // 128 fp32 rescale factors and a flag word (with panel 0)
 constexpr int kFinBytes = 128 * 2 * 4;     // final (m, l) per head
 constexpr int kThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2..9 row warps
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -64,21 +68,22 @@ constexpr uint32_t kOCol = 0;              // value CTA TMEM: O (512 columns)
 
 // Shared memory (offsets from the 1024-byte aligned dynamic base).
 //   score CTA
-constexpr int S_RING = 0;                              // kRing x 16 KB (Q is staged in slots 0..8 first)
-constexpr int S_STAGE = S_RING + kRing * kSlice;       // 2 x kMsgSlot: P panels + header, send side
-constexpr int S_MX = S_STAGE + 2 * kMsgSlot;           // [2 tiles][2 halves][128] fp32 maxima, then l halves
-constexpr int S_FIN = S_MX + 2 * 2 * 128 * 4;          // final (m, l) per head
-constexpr int S_END = S_FIN + kFinBytes;
+constexpr int S_RING = 0;                              // kRing x 48 KB (Q is staged in slots 0..2 first)
+constexpr int S_PANEL = S_RING + kRing * kGroup;       // 2 x 16 KB P panels, send side
+constexpr int S_HDR = S_PANEL + 2 * kPanel;            // rescale factors + flag sent with panel 0
+constexpr int S_MX = S_HDR + 1024;                     // [2 halves][128] fp32: tile maxima, then l halves
+constexpr int S_END = S_MX + 2 * 128 * 4;
 //   value CTA
 constexpr int V_CST = 0;                               // kCStages x 64 KB
-constexpr int V_MSG = V_CST + kCStages * kCStage;      // 2 x kMsgSlot receive side; the final (m, l) lands in slot 0
-constexpr int V_END = V_MSG + 2 * kMsgSlot;
+constexpr int V_PANEL = V_CST + kCStages * kCStage;    // 2 x 16 KB P panels, receive side; the final (m, l) lands in panel 0
+constexpr int V_HDR = V_PANEL + 2 * kPanel;
+constexpr int V_END = V_HDR + 1024;
 //   both (same offset in both CTAs: remote arrivals and copies address it by offset)
 constexpr int OFF_BAR = (S_END > V_END ? S_END : V_END);
 enum Bar {
-  SB_SLOT_FULL = 0,                       // [kRing] score: slice landed
-  SB_SLOT_EMPTY = SB_SLOT_FULL + kRing,   // [kRing] score: QK MMAs done with the slice
-  SB_QFULL = SB_SLOT_EMPTY + kRing,       // score: Q landed in slots 0..8
+  SB_SLOT_FULL = 0,                       // [kRing] score: slice group landed
+  SB_SLOT_EMPTY = SB_SLOT_FULL + kRing,   // [kRing] score: QK MMAs done with the group
+  SB_QFULL = SB_SLOT_EMPTY + kRing,       // score: Q landed in slots 0..2
   SB_QREADY = SB_QFULL + 1,               // score: Q copied into TMEM (256)
   SB_SFULL = SB_QREADY + 1,               // score: S written
   SB_SFREE = SB_SFULL + 1,                // score: S read by the softmax threads (256)
@@ -96,7 +101,7 @@ enum Bar {
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;   // tmem base, abort flag, command word, O-initialised flag
 constexpr int kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(S_STAGE % 1024 == 0 && V_MSG % 1024 == 0 && kMsgSlot % 1024 == 0, "panel alignment");
+static_assert(S_PANEL % 1024 == 0 && V_PANEL % 1024 == 0 && kGroup % 1024 == 0, "swizzle alignment");
 
 enum Cmd { CMD_ZERO = 1, CMD_RESCALE = 2, CMD_DONE = 4 };
 
@@ -153,18 +158,19 @@ __device__ __forceinline__ void give_up(const DecodeParams& p, volatile int* abo
   st_cluster_u32(mapa(smem_u32(smem + OFF_MISC + 4), peer), 1u);
 }
 
-// Slot and use index of score slice k (tile k / 9, column box k % 9). Q occupies slots
-// 0..8 before the first cache slice, so slice k goes to slot (9 + k) % kRing and that
-// slot has held (9 + k) / kRing - [slot < 9] cache slices before it.
-__device__ __forceinline__ int slice_slot(int k) { return (9 + k) % kRing; }
-__device__ __forceinline__ int slice_prior_uses(int k) {
-  const int r = slice_slot(k);
-  return (9 + k) / kRing - (r < 9 ? 1 : 0);
+// Slot and use index of score group k (tile k / 3, column chunks 3 (k % 3) .. +2). Q
+// occupies slots 0..2 before the first cache group, so group k goes to slot
+// (3 + k) % kRing and that slot has held (3 + k) / kRing - [slot < 3] cache groups before.
+__device__ __forceinline__ int group_slot(int k) { return (3 + k) % kRing; }
+__device__ __forceinline__ int group_prior_uses(int k) {
+  const int r = group_slot(k);
+  return (3 + k) / kRing - (r < 3 ? 1 : 0);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
-                 const __grid_constant__ CUtensorMap qmap, float scale_log2) {
+decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
+                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
+                 float scale_log2) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
@@ -223,8 +229,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
     mbar_init(&bars[VB_CREQ], 1);
     mbar_init(&bars[VB_CDONE], 256);
     if (rank == 1) {   // the first tile's P panels and the final message may arrive any time after the cluster sync
-      mbar_arrive_expect_tx(&bars[VB_PFULL], kMsg);
-      mbar_arrive_expect_tx(&bars[VB_PFULL + 1], kMsg);
+      mbar_arrive_expect_tx(&bars[VB_PFULL], kPanel + kHdr);
+      mbar_arrive_expect_tx(&bars[VB_PFULL + 1], kPanel);
       mbar_arrive_expect_tx(&bars[VB_FIN], kFinBytes);
     }
     fence_mbar_init_cluster();
@@ -243,40 +249,56 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
     // =============================== score CTA =========================================
     if (warp == 0) {
       if (lane == 0) {
-        // ---- TMA producer: Q, then the column slices of every tile ----
+        // ---- TMA producer: Q, then three column slices of a tile per instruction ----
         const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_last = l2_policy_evict_last();   // c_KV is read again by the value CTA
-        prefetch_tmap(&cmap);
+        prefetch_tmap(&smap);
         prefetch_tmap(&qmap);
         const int qrows = p.n_h < 128 ? p.n_h : 128;
         mbar_arrive_expect_tx(&bars[SB_QFULL], 9 * qrows * 128);
-        for (int c = 0; c < 9; ++c)
-          tma_load_2d(smem + S_RING + c * kSlice, &qmap, &bars[SB_QFULL], 64 * c, b * p.n_h, pol_first);
+        for (int g = 0; g < 3; ++g)
+          tma_load_3d(smem + S_RING + g * kGroup, &qmap, &bars[SB_QFULL], 0, b * p.n_h, 3 * g, pol_first);
+        const bool paged = p.block_table != nullptr;
         int issued = 0;
         HalfInfo h0{}, h1{};
-        for (int k = 0; k < 9 * n_tiles; ++k) {
-          const int i = k / 9, c = k % 9;
-          const int r = slice_slot(k), prior = slice_prior_uses(k);
+        for (int k = 0; k < 3 * n_tiles; ++k) {
+          const int i = k / 3, g = k % 3;
+          const int r = group_slot(k), prior = group_prior_uses(k);
           bool ok = true;
-          if (r < 9 && prior == 0) ok = mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs);
+          if (r < 3 && prior == 0) ok = mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs);
           if (ok && prior > 0) ok = mbar_wait(&bars[SB_SLOT_EMPTY + r], (prior - 1) & 1, abort_flag, kWaitNs);
           if (!ok) {
             give_up(p, abort_flag, smem, peer);
             break;
           }
-          if (c == 0) {
+          if (g == 0) {
             h0 = half_info(p, b, st, en, 2 * i, true);
             h1 = half_info(p, b, st, en, 2 * i + 1, true);
           }
-          const uint32_t bytes = (h0.load ? kBox : 0) + (h1.load ? kBox : 0);
-          unsigned char* dst = smem + S_RING + r * kSlice;
-          const uint64_t pol = c < 8 ? pol_last : pol_first;
-          if (bytes) {
-            mbar_arrive_expect_tx(&bars[SB_SLOT_FULL + r], bytes);
-            if (h0.load) tma_load_2d(dst, &cmap, &bars[SB_SLOT_FULL + r], 64 * c, h0.row0, pol);
-            if (h1.load) tma_load_2d(dst + kBox, &cmap, &bars[SB_SLOT_FULL + r], 64 * c, h1.row0, pol);
+          unsigned char* dst = smem + S_RING + r * kGroup;
+          const uint64_t pol = g < 2 ? pol_last : pol_first;   // chunk 8 (the RoPE key) is read once
+          if (!paged) {
+            // 128 consecutive rows: one 3D box (the rows past a ragged end are masked)
+            if (h0.load) {
+              mbar_arrive_expect_tx(&bars[SB_SLOT_FULL + r], kGroup);
+              tma_load_3d(dst, &smap, &bars[SB_SLOT_FULL + r], 0, h0.row0, 3 * g, pol);
+            } else {
+              mbar_arrive(&bars[SB_SLOT_FULL + r]);
+            }
           } else {
-            mbar_arrive(&bars[SB_SLOT_FULL + r]);
+            // two pages: one 64-row box per page and column chunk (slice c: page 0 rows
+            // at +0, page 1 rows at +8 KB)
+            const uint32_t bytes = 3 * ((h0.load ? kBox : 0) + (h1.load ? kBox : 0));
+            if (bytes) {
+              mbar_arrive_expect_tx(&bars[SB_SLOT_FULL + r], bytes);
+              for (int c = 0; c < 3; ++c) {
+                if (h0.load) tma_load_3d(dst + c * kSlice, &smap, &bars[SB_SLOT_FULL + r], 0, h0.row0, 3 * g + c, pol);
+                if (h1.load)
+                  tma_load_3d(dst + c * kSlice + kBox, &smap, &bars[SB_SLOT_FULL + r], 0, h1.row0, 3 * g + c, pol);
+              }
+            } else {
+              mbar_arrive(&bars[SB_SLOT_FULL + r]);
+            }
           }
           issued = k + 1;
         }
@@ -284,7 +306,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
         const volatile int never = 0;
         mbar_wait(&bars[SB_QFULL], 0, &never, kWaitNs / 4);
         for (int k = max(0, issued - kRing); k < issued; ++k)
-          mbar_wait(&bars[SB_SLOT_FULL + slice_slot(k)], slice_prior_uses(k) & 1, &never, kWaitNs / 4);
+          mbar_wait(&bars[SB_SLOT_FULL + group_slot(k)], group_prior_uses(k) & 1, &never, kWaitNs / 4);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -297,18 +319,20 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
             break;
           }
           tc_fence_after();
-          for (int c = 0; c < 9; ++c) {
-            const int k = 9 * i + c, r = slice_slot(k);
-            if (!mbar_wait(&bars[SB_SLOT_FULL + r], slice_prior_uses(k) & 1, abort_flag, kWaitNs)) {
+          for (int g = 0; g < 3; ++g) {
+            const int k = 3 * i + g, r = group_slot(k);
+            if (!mbar_wait(&bars[SB_SLOT_FULL + r], group_prior_uses(k) & 1, abort_flag, kWaitNs)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t base = smem_u32(smem + S_RING + r * kSlice);
+            const uint32_t base = smem_u32(smem + S_RING + r * kGroup);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kSCol, tmem + kQCol + 8 * (4 * c + kk), sdesc_sw128(base + 32 * kk, 16, 1024), idq,
-                     (c | kk) ? 1u : 0u);
+            for (int c = 0; c < 3; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tmem + kSCol, tmem + kQCol + 8 * (4 * (3 * g + c) + kk),
+                       sdesc_sw128(base + c * kSlice + 32 * kk, 16, 1024), idq, (g | c | kk) ? 1u : 0u);
             mma_commit(&bars[SB_SLOT_EMPTY + r]);
           }
           if (!ok) break;
@@ -330,7 +354,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
 #pragma unroll 1
         for (int c = j; c < 9; c += 2) {
           uint32_t r[32];
-          const unsigned char* row = smem + S_RING + c * kSlice + h * 128;
+          const unsigned char* row = smem + S_RING + (c / 3) * kGroup + (c % 3) * ((p.n_h < 128 ? p.n_h : 128) * 128) + h * 128;
 #pragma unroll
           for (int x = 0; x < 8; ++x) {
             const uint4 v = h < p.n_h ? *reinterpret_cast<const uint4*>(row + ((x ^ (h & 7)) << 4))
@@ -348,7 +372,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
 
       float m_run = -INFINITY, l_run = 0.f;
       float* mx = reinterpret_cast<float*>(smem + S_MX);
-      const uint32_t msg_remote = mapa(smem_u32(smem + V_MSG + j * kMsgSlot), 1);
+      const uint32_t panel_remote = mapa(smem_u32(smem + V_PANEL + j * kPanel), 1);
+      const uint32_t hdr_remote = mapa(smem_u32(smem + V_HDR), 1);
       const uint32_t pfull_remote = mapa(smem_u32(&bars[VB_PFULL + j]), 1);
       // Every thread runs every iteration and every named barrier; after an abort the
       // waits return at once and the tiles are processed as fully masked.
@@ -376,11 +401,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
         float fac = 1.f;
         bool row_rescale = false;
         const uint32_t nneed = named_popc(1, 256, mt > m_run + kRescaleLog2);
-        if (nneed) {
-          float* mxb = mx + (i & 1) * 256;
-          mxb[j * 128 + h] = mt;
+        if (nneed) {   // mx is reused from tile to tile: the vote above orders it
+          mx[j * 128 + h] = mt;
           named_sync(1, 256);
-          const float mrow = fmaxf(mxb[h], mxb[128 + h]);
+          const float mrow = fmaxf(mx[h], mx[128 + h]);
           if (mrow > m_run + kRescaleLog2) {
             if (m_run != -INFINITY) {
               fac = ex2(m_run - mrow);
@@ -406,35 +430,35 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
         l_run += lsum;
         // The staging panel is free once the value CTA's PV on the previous tile has read it.
         if (i > 0) mbar_wait<true>(&bars[SB_PFREE + j], (i - 1) & 1, abort_flag, kWaitNs);
-        unsigned char* stg = smem + S_STAGE + j * kMsgSlot;
+        unsigned char* stg = smem + S_PANEL + j * kPanel;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(stg + h * 128 + ((c ^ (h & 7)) << 4)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         if (j == 0) {
-          reinterpret_cast<float*>(stg + kPanel)[h] = fac;
-          if (h == 0) reinterpret_cast<uint32_t*>(stg + kPanel + 512)[0] = nres;
+          reinterpret_cast<float*>(smem + S_HDR)[h] = fac;
+          if (h == 0) reinterpret_cast<uint32_t*>(smem + S_HDR + 512)[0] = nres;
         }
         fence_proxy_async_smem();
         named_sync(2 + j, 128);
-        if (q == 0 && lane == 0 && !*abort_flag) bulk_copy_to_peer(msg_remote, stg, kMsg, pfull_remote);
+        if (q == 0 && lane == 0 && !*abort_flag) {
+          bulk_copy_to_peer(panel_remote, stg, kPanel, pfull_remote);
+          if (j == 0) bulk_copy_to_peer(hdr_remote, smem + S_HDR, kHdr, pfull_remote);
+        }
       }
-      // final (m, l) of each head → the value CTA, once its last PV has read both panels
+      // final (m, l) of each head → the value CTA's panel 0, once its last PV has read it
       named_sync(1, 256);
       mx[j * 128 + h] = l_run;
       named_sync(1, 256);
-      float* fin = reinterpret_cast<float*>(smem + S_FIN);
       if (j == 0) {
+        float* fin = reinterpret_cast<float*>(smem + S_PANEL);
+        const bool ok = mbar_wait<true>(&bars[SB_PFREE], (n_tiles - 1) & 1, abort_flag, kWaitNs);
         fin[2 * h] = m_run;
         fin[2 * h + 1] = mx[h] + mx[128 + h];
-      }
-      fence_proxy_async_smem();
-      named_sync(1, 256);
-      if (warp == 2 && lane == 0) {
-        bool ok = mbar_wait<true>(&bars[SB_PFREE], (n_tiles - 1) & 1, abort_flag, kWaitNs) &&
-                  mbar_wait<true>(&bars[SB_PFREE + 1], (n_tiles - 1) & 1, abort_flag, kWaitNs);
-        if (ok && !*abort_flag)
-          bulk_copy_to_peer(mapa(smem_u32(smem + V_MSG), 1), fin, kFinBytes, mapa(smem_u32(&bars[VB_FIN]), 1));
+        fence_proxy_async_smem();
+        named_sync(2, 128);
+        if (q == 0 && lane == 0 && ok && !*abort_flag)
+          bulk_copy_to_peer(mapa(smem_u32(smem + V_PANEL), 1), fin, kFinBytes, mapa(smem_u32(&bars[VB_FIN]), 1));
       }
     }
   } else {
@@ -443,7 +467,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
       if (lane == 0) {
         // ---- TMA producer: c_KV of every 64-token step (evict-first: last reader) ----
         const uint64_t pol = l2_policy_evict_first();
-        prefetch_tmap(&cmap);
+        prefetch_tmap(&vmap);
         int issued = 0;
         for (int u = 0; u < n_halves; ++u) {
           const int sg = u % kCStages;
@@ -455,9 +479,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
           const HalfInfo hi = half_info(p, b, st, en, u, false);
           if (hi.load) {
             mbar_arrive_expect_tx(&bars[VB_CFULL + sg], kCStage);
-            unsigned char* dst = smem + V_CST + sg * kCStage;
-            for (int c = 0; c < 8; ++c)
-              tma_load_2d(dst + c * kBox, &cmap, &bars[VB_CFULL + sg], 64 * c, hi.row0, pol);
+            tma_load_3d(smem + V_CST + sg * kCStage, &vmap, &bars[VB_CFULL + sg], 0, hi.row0, 0, pol);
           } else {
             mbar_arrive(&bars[VB_CFULL + sg]);
           }
@@ -481,11 +503,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
             ok = false;
             break;
           }
-          if (i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[VB_PFULL + j], kMsg);   // next tile's panel j
+          if (i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[VB_PFULL + j], j == 0 ? kPanel + kHdr : kPanel);
           const HalfInfo hi = half_info(p, b, st, en, u, false);
-          const unsigned char* msg = smem + V_MSG + j * kMsgSlot;
+          const unsigned char* msg = smem + V_PANEL + j * kPanel;
           int c = 0;
-          if (j == 0 && o_init && *reinterpret_cast<const volatile uint32_t*>(msg + kPanel + 512) != 0u)
+          if (j == 0 && o_init && *reinterpret_cast<const volatile uint32_t*>(smem + V_HDR + 512) != 0u)
             c |= CMD_RESCALE;
           if (hi.nvalid > 0 && hi.nvalid < kHalf) c |= CMD_ZERO;
           if (c) {
@@ -560,7 +582,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
         }
         if (c & CMD_RESCALE) {
           tc_fence_after();
-          const float f = reinterpret_cast<const float*>(smem + V_MSG + kPanel)[h];
+          const float f = reinterpret_cast<const float*>(smem + V_HDR)[h];
           if (__any_sync(0xffffffffu, f != 1.f)) {
             uint32_t r[32];
 #pragma unroll 1
@@ -582,7 +604,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap cmap,
       // (the c_KV stages are idle now) so that the global stores are coalesced rows
       const bool fin_ok = ok && warp_wait<true>(&bars[VB_FIN], 0, abort_flag);
       tc_fence_after();
-      const float* fin = reinterpret_cast<const float*>(smem + V_MSG);
+      const float* fin = reinterpret_cast<const float*>(smem + V_PANEL);
       const float m = fin[2 * h];
       const float l = fin[2 * h + 1];
       const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
@@ -640,15 +662,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D map over rows of 576 bf16 with boxes of `box_rows` rows x 64 columns (128B swizzle).
-bool make_row_map(const void* base, int64_t rows, int box_rows, CUtensorMap* map) {
+// 3D map over rows of 576 bf16 seen as (64 columns, row, 64-column chunk), the chunk
+// stride being 128 bytes; a box of `box_rows` rows x `box_chunks` chunks lands in
+// shared memory chunk-major, each chunk a 128B-swizzled [box_rows][64] block.
+bool make_row_map(const void* base, int64_t rows, int box_rows, int box_chunks, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -661,9 +685,13 @@ bool decode_tc_supported(const DecodeParams& p) {
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_t st) {
   (void)max_seq_len;
-  CUtensorMap cmap, qmap;
-  if (!make_row_map(p.data, p.num_rows, 64, &cmap)) return cudaErrorInvalidValue;
-  if (!make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, &qmap)) return cudaErrorInvalidValue;
+  // score side: 128 rows x 3 chunks (contiguous) or, for paged caches, 64 rows x 1 chunk
+  // through the value map; value side: 64 rows x 8 chunks; queries: n_h rows x 3 chunks
+  CUtensorMap smap, vmap, qmap;
+  if (!make_row_map(p.data, p.num_rows, p.block_table ? 64 : kTile, p.block_table ? 1 : 3, &smap) ||
+      !make_row_map(p.data, p.num_rows, 64, 8, &vmap) ||
+      !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap))
+    return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -672,7 +700,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   if (attr_err != cudaSuccess) return attr_err;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t ctas = 2ll * p.B * p.S;
-  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, cmap, qmap, scale_log2);
+  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, smap, vmap, qmap, scale_log2);
   return cudaGetLastError();
 }
 

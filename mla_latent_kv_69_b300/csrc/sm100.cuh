@@ -315,3 +315,17 @@ __device__ __forceinline__ uint32_t named_popc(uint32_t id, uint32_t count, bool
                : "memory")
 }  // namespace sm100
 }  // namespace mla
+
+namespace mla {
+namespace sm100 {
+// 3D tiled load into this CTA's shared memory; completes bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+}  // namespace sm100
+}  // namespace mla
