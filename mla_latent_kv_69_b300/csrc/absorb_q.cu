@@ -1,75 +1,236 @@
 // mla_absorb_q: q_lat[b,h] = [ W_UK[h]^T q^C[b,h] ‖ RoPE(q^R[b,h], pos[b]) ].
 // "DeepSeek-V2 机制拆解" (discosf.com), §长上下文推理的第一瓶颈 (W_UK folded into the
 // query side) and §解耦 RoPE 与 YaRN (the 64-wide decoupled query carries position).
+//
+// Per head the absorbed query is a small GEMM with the latent dimension as M:
+//     q_lat[b, h, j] = sum_d W_UK[h, d, j] q^C[b, h, d]      (M = 512 j, N = batch, K = 128 d)
+// One CTA per (head, tile of up to 128 sequences). The four 32 KB M-tiles of W_UK[h]
+// (an MN-major operand: j is contiguous) and the batch tile of q^C arrive by TMA, each
+// M-tile on its own barrier so the tensor core starts on the first while the rest land;
+// tcgen05 accumulates four 128 x N fp32 tiles in TMEM and the epilogue rounds them to
+// bf16. The weight bytes dominate: W_UK is read from HBM once per call.
+//
+// The decoupled part is rotated on CUDA cores. Pair (i, i + 32) turns by
+// theta_i = pos * base^(-2i/64); positions reach 131071, where an fp32 product would
+// be off by ~1e-2 rad, so the angle is reduced exactly: f_i = base^(-2i/64) / (2 pi) is
+// held as a 64-bit fixed-point fraction (computed on the host in double), the turn
+// count's fraction is the wrapping 64-bit product pos * f_i, and only the reduced angle
+// goes through fp32 sincos.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kAbsorbBT = 16;       // batch rows sharing one pass over W_UK[h]
-constexpr int kAbsorbThreads = 256; // 2 output columns per thread → 512
+using namespace sm100;
 
-__global__ void __launch_bounds__(kAbsorbThreads)
-absorb_q_simt(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ w_uk,
-              const int32_t* __restrict__ pos, int B, int n_h, float rope_base,
-              __nv_bfloat16* __restrict__ q_lat) {
-  __shared__ float qs[kAbsorbBT][kNope];
-  const int h = blockIdx.x;
-  const int b0 = blockIdx.y * kAbsorbBT;
-  const int nb = min(kAbsorbBT, B - b0);
-  for (int i = threadIdx.x; i < kAbsorbBT * kNope; i += blockDim.x) {
-    int bi = i / kNope, d = i % kNope;
-    qs[bi][d] = bi < nb ? __bfloat162float(q[((int64_t)(b0 + bi) * n_h + h) * kQ + d]) : 0.f;
+constexpr int kNB = 128;                     // sequences per CTA (the MMA N, padded to 16)
+constexpr int kThreads = 128;
+constexpr int kWTile = 2 * 128 * 128;        // one M-tile of W_UK[h]: two 64-j chunks x 128 d rows (32 KB)
+constexpr int OFF_W = 0;                     // four M-tiles
+constexpr int OFF_Q = 4 * kWTile;            // q^C tile: two 64-d chunks x 128 rows x 128 B
+constexpr int OFF_BAR = OFF_Q + 2 * kNB * 128;
+constexpr int kSmem = OFF_BAR + 64;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct RopeTurns {
+  unsigned long long f[kRope / 2];   // base^(-2i/64) / (2 pi) as an unsigned 0.64 fixed-point fraction
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
+            const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int B, int n_h,
+            const RopeTurns turns, __nv_bfloat16* __restrict__ q_lat) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int h = blockIdx.x, b0 = blockIdx.y * kNB;
+  const int nb = min(kNB, B - b0);
+  const int N = (nb + 15) & ~15;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [0..3] W M-tiles, [4] q tile, [5] MMAs done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 48);
+  volatile int* ok_word = reinterpret_cast<volatile int*>(smem + OFF_BAR + 52);
+  const bool aligned = (smem_u32(smem) & 1023u) == 0;   // the 128B swizzle needs 1024-byte aligned tiles
+
+  if (aligned) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+      *ok_word = 0;
+      fence_mbar_init_cluster();
+    }
+    if (warp == 0) {
+      tmem_alloc(tmem_slot, 512);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (aligned) {
+    const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      prefetch_tmap(&qmap);
+      prefetch_tmap(&wmap);
+      mbar_arrive_expect_tx(&bars[4], 2 * kNB * 128);
+      tma_load_4d(smem + OFF_Q, &qmap, &bars[4], 0, h, b0, 0, pol);
+      for (int mt = 0; mt < 4; ++mt) {
+        mbar_arrive_expect_tx(&bars[mt], kWTile);
+        tma_load_3d(smem + OFF_W + mt * kWTile, &wmap, &bars[mt], 0, h * kNope, 2 * mt, pol);
+      }
+      const uint32_t idesc = idesc_f16(128, N, false, /*a_mn=*/true, /*b_mn=*/false);
+      const volatile int never = 0;
+      bool ok = mbar_wait(&bars[4], 0, &never, kWaitNs);
+      for (int mt = 0; ok && mt < 4; ++mt) {
+        ok = mbar_wait(&bars[mt], 0, &never, kWaitNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t wt = smem_u32(smem + OFF_W + mt * kWTile);
+        const uint32_t qt = smem_u32(smem + OFF_Q);
+#pragma unroll
+        for (int kk = 0; kk < kNope / 16; ++kk) {
+          // A: 16 d rows of 128 B (64 j) per 64-j chunk, chunks 16 KB apart; B: q rows, K-major
+          const uint64_t a = sdesc_sw128(wt + kk * 2048, 128 * 128, 1024);
+          const uint64_t bq = sdesc_sw128(qt + (kk >> 2) * (kNB * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + 128 * mt, a, bq, idesc, kk > 0 ? 1u : 0u);
+        }
+      }
+      *ok_word = ok ? 1 : 0;
+      mma_commit(&bars[5]);
+      // loads still in flight land before the CTA may leave
+      mbar_wait(&bars[4], 0, &never, kWaitNs / 4);
+      for (int mt = 0; mt < 4; ++mt) mbar_wait(&bars[mt], 0, &never, kWaitNs / 4);
+    }
+
+    // decoupled query, overlapping the tensor-core work: thread (n, g) rotates pairs
+    // 8g .. 8g+7 of sequence n; every load of a pass is issued before any math
+#pragma unroll 1
+    for (int n0 = 0; n0 < nb; n0 += kThreads / 4) {
+      const int n = n0 + (threadIdx.x >> 2), g = threadIdx.x & 3;
+      if (n < nb) {
+        const int64_t row = (int64_t)(b0 + n) * n_h + h;
+        const uint4 u1 = *reinterpret_cast<const uint4*>(q + row * kQ + kNope + 8 * g);
+        const uint4 u2 = *reinterpret_cast<const uint4*>(q + row * kQ + kNope + kRope / 2 + 8 * g);
+        const unsigned long long ps = (unsigned long long)(long long)pos[b0 + n];
+        const __nv_bfloat162* x1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
+        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&u2);
+        uint32_t o1[4], o2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a1 = __bfloat1622float2(x1[e]), a2 = __bfloat1622float2(x2[e]);
+          float r1[2], r2[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int i = 8 * g + 2 * e + k;
+            const unsigned long long frac = ps * turns.f[i];
+            const float ang = (float)(frac >> 40) * (6.283185307179586f / 16777216.f);
+            float sn, cs;
+            sincosf(ang, &sn, &cs);
+            const float y1 = k ? a1.y : a1.x, y2 = k ? a2.y : a2.x;
+            r1[k] = y1 * cs - y2 * sn;
+            r2[k] = y2 * cs + y1 * sn;
+          }
+          const __nv_bfloat162 v1 = __floats2bfloat162_rn(r1[0], r1[1]);
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(r2[0], r2[1]);
+          o1[e] = *reinterpret_cast<const uint32_t*>(&v1);
+          o2[e] = *reinterpret_cast<const uint32_t*>(&v2);
+        }
+        __nv_bfloat16* out = q_lat + row * kRow + kLatent;
+        *reinterpret_cast<uint4*>(out + 8 * g) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *reinterpret_cast<uint4*>(out + kRope / 2 + 8 * g) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+      }
+    }
+
+    __syncthreads();   // orders ok_word
+
+    // epilogue: lane j of M-tile mt holds q_lat[b0 + n, h, 128 mt + j] in column n
+    const volatile int never = 0;
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bars[5], 0, &never, kWaitNs));
+    tc_fence_after();
+    if (done && *ok_word) {
+      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+        const int j = 128 * mt + 32 * warp + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < N; c0 += 32) {
+          uint32_t r[32];
+          MLA_TMEM_LD32(trow + 128 * mt + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (c0 + x < nb)
+              q_lat[((int64_t)(b0 + c0 + x) * n_h + h) * kRow + j] = __float2bfloat16_rn(__uint_as_float(r[x]));
+        }
+      }
+    }
+    tc_fence_before();
   }
   __syncthreads();
+  tc_fence_after();
+  if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 512);
+}
 
-  const int c = threadIdx.x * 2;
-  float acc[kAbsorbBT][2];
-#pragma unroll
-  for (int bi = 0; bi < kAbsorbBT; ++bi) acc[bi][0] = acc[bi][1] = 0.f;
-  const __nv_bfloat162* w =
-      reinterpret_cast<const __nv_bfloat162*>(w_uk + (int64_t)h * kNope * kLatent + c);
-  for (int d = 0; d < kNope; ++d) {
-    float2 wv = __bfloat1622float2(w[d * (kLatent / 2)]);
-#pragma unroll
-    for (int bi = 0; bi < kAbsorbBT; ++bi) {
-      acc[bi][0] = fmaf(qs[bi][d], wv.x, acc[bi][0]);
-      acc[bi][1] = fmaf(qs[bi][d], wv.y, acc[bi][1]);
-    }
-  }
-#pragma unroll
-  for (int bi = 0; bi < kAbsorbBT; ++bi) {
-    if (bi < nb) {
-      *reinterpret_cast<__nv_bfloat162*>(q_lat + ((int64_t)(b0 + bi) * n_h + h) * kRow + c) =
-          __floats2bfloat162_rn(acc[bi][0], acc[bi][1]);
-    }
-  }
-
-  // Decoupled query: rotate-half pairs (i, i+32), angle pos * base^(-i/32). The angle
-  // and its sine/cosine are taken in fp64: positions reach 131071 rad on pair 0.
-  if (threadIdx.x < kRope / 2) {
-    const int i = threadIdx.x;
-    const double inv_freq = pow((double)rope_base, -2.0 * i / (double)kRope);
-    for (int bi = 0; bi < nb; ++bi) {
-      const int b = b0 + bi;
-      double sn, cs;
-      sincos((double)pos[b] * inv_freq, &sn, &cs);
-      const __nv_bfloat16* qr = q + ((int64_t)b * n_h + h) * kQ + kNope;
-      const double x1 = __bfloat162float(qr[i]);
-      const double x2 = __bfloat162float(qr[i + kRope / 2]);
-      __nv_bfloat16* out = q_lat + ((int64_t)b * n_h + h) * kRow + kLatent;
-      out[i] = __float2bfloat16_rn((float)(x1 * cs - x2 * sn));
-      out[i + kRope / 2] = __float2bfloat16_rn((float)(x2 * cs + x1 * sn));
-    }
-  }
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult qr;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
 }
 
 }  // namespace
 
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const int32_t* pos,
                             int B, int n_h, float rope_base, __nv_bfloat16* q_lat, cudaStream_t st) {
-  dim3 grid(n_h, ceil_div(B, kAbsorbBT));
-  absorb_q_simt<<<grid, kAbsorbThreads, 0, st>>>(q, w_uk, pos, B, n_h, rope_base, q_lat);
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  // W_UK viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = one M-tile (2 chunks)
+  CUtensorMap wmap, qmap;
+  {
+    cuuint64_t dims[3] = {64, (cuuint64_t)n_h * kNope, kLatent / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, 128};
+    cuuint32_t box[3] = {64, kNope, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (fn(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(w_uk), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // q viewed as (64 d, head, sequence, 64-d chunk); box = one head, 128 sequences, q^C's 2 chunks
+  {
+    cuuint64_t dims[4] = {64, (cuuint64_t)n_h, (cuuint64_t)B, 3};
+    cuuint64_t strides[3] = {(cuuint64_t)kQ * 2, (cuuint64_t)n_h * kQ * 2, 128};
+    cuuint32_t box[4] = {64, 1, kNB, 2};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<__nv_bfloat16*>(q), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  RopeTurns turns;
+  for (int i = 0; i < kRope / 2; ++i) {
+    const double f = std::pow((double)rope_base, -2.0 * i / (double)kRope) / (2.0 * M_PI);   // < 1/(2 pi)
+    turns.f[i] = (unsigned long long)std::ldexp(f, 64);
+  }
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(absorb_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  dim3 grid(n_h, ceil_div(B, kNB));
+  absorb_q_tc<<<grid, kThreads, kSmem, st>>>(wmap, qmap, q, pos, B, n_h, turns, q_lat);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,9 @@
 // The TMA engine spends a roughly fixed time per box row, so loads use 3D tensor maps
 // (64 columns x rows x column chunks) that fetch several 128-byte chunks of each row
 // per instruction; the shared-memory image is the same chunk-major 128B-swizzled
-// layout as one 2D box per chunk.
+// layout as one 2D box per chunk. The value CTA starts loading only once the score
+// CTA holds Q (the query load goes first), and its epilogue stages O in swizzled
+// shared memory and writes it with 3D TMA stores.
 // A tensor-core instruction costs at least ~64 cycles whatever N <= 128, so the score
 // side uses N = 128 token tiles; the shared-memory link between the two SMs is narrow
 // (~20 B/clk), so only P (16 KB per 64 tokens) crosses it, never fp32 scores.
@@ -96,7 +98,8 @@ enum Bar {
   VB_FLUSH = VB_FIN + 1,                  // value MMA warp: all MMAs done
   VB_CREQ = VB_FLUSH + 1,                 // value: command for the row warps (1)
   VB_CDONE = VB_CREQ + 1,                 // value: row warps finished it (256)
-  B_COUNT = VB_CDONE + 1
+  VB_GO = VB_CDONE + 1,                   // value: the score CTA holds Q (remote arrival)
+  B_COUNT = VB_GO + 1
 };
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;   // tmem base, abort flag, command word, O-initialised flag
 constexpr int kSmemBytes = OFF_MISC + 16;
@@ -170,6 +173,7 @@ __device__ __forceinline__ int group_prior_uses(int k) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
+                 const __grid_constant__ CUtensorMap omap,
                  float scale_log2) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = cluster_ctarank();
@@ -228,6 +232,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
     mbar_init(&bars[VB_FLUSH], 1);
     mbar_init(&bars[VB_CREQ], 1);
     mbar_init(&bars[VB_CDONE], 256);
+    mbar_init(&bars[VB_GO], 1);
     if (rank == 1) {   // the first tile's P panels and the final message may arrive any time after the cluster sync
       mbar_arrive_expect_tx(&bars[VB_PFULL], kPanel + kHdr);
       mbar_arrive_expect_tx(&bars[VB_PFULL + 1], kPanel);
@@ -313,6 +318,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         // ---- S = Q · C^T, 36 MMAs of 128 x 128 x 16 per tile ----
         const uint32_t idq = idesc_f16(128, kTile, false, false, false);
         bool ok = mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs);
+        if (ok) mbar_arrive_remote(&bars[VB_GO], 1);   // the value CTA may start its loads
         for (int i = 0; ok && i < n_tiles; ++i) {
           if (i > 0 && !mbar_wait(&bars[SB_SFREE], (i - 1) & 1, abort_flag, kWaitNs)) {
             ok = false;
@@ -389,13 +395,20 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         tc_fence_before();
         mbar_arrive(&bars[SB_SFREE]);
         const int nv = got ? half_info(p, b, st, en, 2 * i + j, false).nvalid : 0;
-        float x[64];
-        float mt = -INFINITY;
+        // Row maximum on the raw scores (the scale is positive); tokens past the split
+        // (ragged tiles only) become -inf so that their weight is exactly 0.
+        if (nv < 64) {
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
-          x[t] = t < nv ? __uint_as_float(sr[t]) * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[t]);
+          for (int t = 0; t < 64; ++t)
+            if (t >= nv) sr[t] = __float_as_uint(-INFINITY);
         }
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sr[k]);
+#pragma unroll
+        for (int t = 8; t < 64; ++t) m8[t & 7] = fmaxf(m8[t & 7], __uint_as_float(sr[t]));
+        const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale_log2;
         // Raise the running maximum only when the tile exceeds it by 2^8 (rare); the
         // two threads of a head agree on the new value through shared memory.
         float fac = 1.f;
@@ -415,17 +428,28 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
           }
         }
         const uint32_t nres = nneed ? named_popc(1, 256, row_rescale) : 0u;
-        const bool live = m_run != -INFINITY;
+        // p = 2^(s * scale - m) as one packed FMA and an SFU exp2 per element; P is
+        // rounded to bf16 for the tensor core, l accumulates the fp32 values.
         uint32_t pk[32];
         float lsum = 0.f;
+        if (m_run != -INFINITY) {
+          const float2 c2 = make_float2(scale_log2, scale_log2);
+          const float2 nm2 = make_float2(-m_run, -m_run);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const float p0 = live ? ex2(x[2 * t] - m_run) : 0.f;
-          const float p1 = live ? ex2(x[2 * t + 1] - m_run) : 0.f;
-          const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-          const float2 back = __bfloat1622float2(v);
-          lsum += back.x + back.y;                 // the sum of exactly the weights the MMA uses
-          pk[t] = *reinterpret_cast<const uint32_t*>(&v);
+          for (int t = 0; t < 32; ++t) {
+            const float2 xy = ffma2(make_float2(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1])), c2, nm2);
+            const float2 pp = make_float2(ex2(xy.x), ex2(xy.y));
+            const __nv_bfloat162 v = __floats2bfloat162_rn(pp.x, pp.y);
+            pk[t] = *reinterpret_cast<const uint32_t*>(&v);
+            acc[t & 3] = fadd2(acc[t & 3], pp);
+          }
+          const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+          lsum = (a01.x + a23.x) + (a01.y + a23.y);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) pk[t] = 0u;
         }
         l_run += lsum;
         // The staging panel is free once the value CTA's PV on the previous tile has read it.
@@ -469,7 +493,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         const uint64_t pol = l2_policy_evict_first();
         prefetch_tmap(&vmap);
         int issued = 0;
-        for (int u = 0; u < n_halves; ++u) {
+        // Start once the score CTA has Q: its query load goes first.
+        if (!mbar_wait<true>(&bars[VB_GO], 0, abort_flag, kWaitNs)) give_up(p, abort_flag, smem, peer);
+        for (int u = 0; u < n_halves && !*abort_flag; ++u) {
           const int sg = u % kCStages;
           if (u >= kCStages &&
               !mbar_wait(&bars[VB_CEMPTY + sg], ((u / kCStages) - 1) & 1, abort_flag, kWaitNs)) {
@@ -609,32 +635,38 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       const float l = fin[2 * h + 1];
       const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
       const float inv = good ? 1.f / l : 0.f;
+      // Two passes of 256 columns; each pass is 8 chunks of 32 fp32, staged chunk-major
+      // and 128B-swizzled ([chunk][head][32]) and written by one 3D TMA store.
+      const int rows = p.n_h < 128 ? p.n_h : 128;
       unsigned char* stg = smem + V_CST;
-      float* obase = p.o_part + ((int64_t)b * p.S + s) * p.n_h * kLatent;
+      const int orow0 = (b * p.S + s) * p.n_h;
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
         uint32_t r[32];
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
-          MLA_TMEM_LD32(trow + kOCol + 256 * pass + 128 * j + 32 * cc, r);
+          const int chunk = 4 * j + cc;
+          MLA_TMEM_LD32(trow + kOCol + 256 * pass + 32 * chunk, r);
           tmem_wait_ld();
+          if (h < rows) {
+            unsigned char* dst = stg + chunk * (rows * 128) + h * 128;
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const int chunk = 32 * j + 8 * cc + x;
-            *reinterpret_cast<float4*>(stg + h * 1024 + ((chunk ^ (h & 7)) << 4)) =
-                make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
-                            __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
+            for (int x = 0; x < 8; ++x)
+              *reinterpret_cast<float4*>(dst + ((x ^ (h & 7)) << 4)) =
+                  make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
+                              __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
           }
         }
+        fence_proxy_async_smem();
         named_sync(1, 256);
-        for (int idx = tid; idx < 128 * 64; idx += 256) {
-          const int row = idx >> 6, ch = idx & 63;
-          if (row < p.n_h)
-            *reinterpret_cast<float4*>(obase + (int64_t)row * kLatent + 256 * pass + 4 * ch) =
-                *reinterpret_cast<const float4*>(stg + row * 1024 + ((ch ^ (row & 7)) << 4));
+        if (tid == 0) {
+          tma_store_3d(&omap, stg, 0, orow0, 8 * pass);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // the staging area is reused by the next pass
         }
         named_sync(1, 256);
       }
+      if (tid == 0) bulk_wait_group0();
       if (j == 0 && h < p.n_h)
         p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] =
             good ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -677,6 +709,20 @@ bool make_row_map(const void* base, int64_t rows, int box_rows, int box_chunks, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D map over the fp32 partial results [rows][512] seen as (32 values, row, 16 chunks of
+// 32), 128B swizzle; a box of `box_rows` rows x 8 chunks is one 256-column half.
+bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)(kLatent / 32)};
+  cuuint64_t strides[2] = {(cuuint64_t)kLatent * 4, 128};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 8};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool decode_tc_supported(const DecodeParams& p) {
@@ -687,10 +733,12 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   (void)max_seq_len;
   // score side: 128 rows x 3 chunks (contiguous) or, for paged caches, 64 rows x 1 chunk
   // through the value map; value side: 64 rows x 8 chunks; queries: n_h rows x 3 chunks
-  CUtensorMap smap, vmap, qmap;
+  // (partial-result store: n_h rows x 8 chunks of 32 fp32)
+  CUtensorMap smap, vmap, qmap, omap;
   if (!make_row_map(p.data, p.num_rows, p.block_table ? 64 : kTile, p.block_table ? 1 : 3, &smap) ||
       !make_row_map(p.data, p.num_rows, 64, 8, &vmap) ||
-      !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap))
+      !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap) ||
+      !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 128 ? p.n_h : 128, &omap))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -700,7 +748,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   if (attr_err != cudaSuccess) return attr_err;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t ctas = 2ll * p.B * p.S;
-  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, smap, vmap, qmap, scale_log2);
+  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, smap, vmap, qmap, omap, scale_log2);
   return cudaGetLastError();
 }
 

@@ -1,54 +1,212 @@
 // mla_up_v: o[b,h,:] = W_UV[h] · o_lat[b,h,:]  (W_UV applied after the latent-space
 // weighted sum; "DeepSeek-V2 机制拆解" (discosf.com), §长上下文推理的第一瓶颈).
+//
+// Per head a small GEMM with the head dimension as M:
+//     o[b, h, d] = sum_j W_UV[h, d, j] o_lat[b, h, j]        (M = 128 d, N = batch, K = 512 j)
+// One CTA per (head, tile of up to 32 sequences). All of W_UV[h] (128 KB, a K-major
+// operand) is requested by TMA at once, four 32 KB boxes of two 64-column chunks on
+// their own barriers. Meanwhile the threads convert the CTA's o_lat rows: the tensor
+// core takes bf16, so each fp32 value is split as hi = bf16(x), lo = bf16(x - hi) and
+// both halves enter the same MMA as 2 x N columns (W·hi + W·lo carries ~16
+// significant bits of o_lat instead of 8). The epilogue adds the two column halves.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kUpBT = 16;          // batch rows per block (W_UV[h] rows reused across them)
-constexpr int kUpWarps = 8;
+using namespace sm100;
 
-__global__ void __launch_bounds__(kUpWarps * 32)
-up_v_simt(const float* __restrict__ o_lat, const __nv_bfloat16* __restrict__ w_uv, int B, int n_h,
-          float* __restrict__ o) {
-  __shared__ float2 os[kUpBT][kLatent / 2];
-  const int h = blockIdx.x;
-  const int b0 = blockIdx.y * kUpBT;
-  const int nb = min(kUpBT, B - b0);
-  for (int i = threadIdx.x; i < kUpBT * (kLatent / 2); i += blockDim.x) {
-    int bi = i / (kLatent / 2), j = i % (kLatent / 2);
-    os[bi][j] = bi < nb ? reinterpret_cast<const float2*>(o_lat + ((int64_t)(b0 + bi) * n_h + h) * kLatent)[j]
-                        : make_float2(0.f, 0.f);
-  }
-  __syncthreads();
+constexpr int kNB = 32;                      // sequences per CTA; MMA N = 2 x round16(nb) <= 64
+constexpr int kThreads = 128;
+constexpr int kChunks = kLatent / 64;        // 8 K-chunks of 64 j
+constexpr int kWBox = 2 * kNope * 128;       // two chunks of W_UV[h]: 128 d rows x 128 j (32 KB)
+constexpr int kXChunk = 2 * kNB * 128;       // one chunk of the (hi, lo) rows: up to 64 rows x 64 j (8 KB)
+constexpr int OFF_W = 0;                     // four boxes = all of W_UV[h]
+constexpr int OFF_X = 4 * kWBox;             // eight chunks
+constexpr int OFF_BAR = OFF_X + kChunks * kXChunk;
+constexpr int kSmem = OFF_BAR + 64;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__global__ void __launch_bounds__(kThreads, 1)
+up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_lat, int B, int n_h,
+        float* __restrict__ o) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int h = blockIdx.x, b0 = blockIdx.y * kNB;
+  const int nb = min(kNB, B - b0);
+  const int NP = (nb + 15) & ~15;   // rows [0, NP) hold hi, [NP, 2 NP) lo
+  const int N = 2 * NP;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int d = warp; d < kNope; d += kUpWarps) {
-    const __nv_bfloat162* wrow =
-        reinterpret_cast<const __nv_bfloat162*>(w_uv + ((int64_t)h * kNope + d) * kLatent);
-    float2 w[kLatent / 64];
-#pragma unroll
-    for (int k = 0; k < kLatent / 64; ++k) w[k] = __bfloat1622float2(wrow[k * 32 + lane]);
-    for (int bi = 0; bi < nb; ++bi) {
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < kLatent / 64; ++k) {
-        float2 v = os[bi][k * 32 + lane];
-        acc = fmaf(w[k].x, v.x, acc);
-        acc = fmaf(w[k].y, v.y, acc);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (lane == 0) o[((int64_t)(b0 + bi) * n_h + h) * kNope + d] = acc;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [0..3] W boxes, [4] X ready, [5] done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 48);
+  volatile int* ok_word = reinterpret_cast<volatile int*>(smem + OFF_BAR + 52);
+  const bool aligned = (smem_u32(smem) & 1023u) == 0;   // the 128B swizzle needs 1024-byte aligned tiles
+
+  if (aligned) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+      mbar_init(&bars[4], kThreads);
+      mbar_init(&bars[5], 1);
+      *ok_word = 1;
+      fence_mbar_init_cluster();
+    }
+    if (warp == 0) {
+      tmem_alloc(tmem_slot, 64);
+      tmem_relinquish();
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (aligned) {
+    const uint32_t tmem = *tmem_slot;
+    const volatile int never = 0;
+    if (threadIdx.x == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      prefetch_tmap(&wmap);
+      for (int i = 0; i < 4; ++i) {
+        mbar_arrive_expect_tx(&bars[i], kWBox);
+        tma_load_3d(smem + OFF_W + i * kWBox, &wmap, &bars[i], 0, h * kNope, 2 * i, pol);
+      }
+    }
+    // o_lat rows → bf16 hi/lo rows of every chunk (K-major, 128B swizzle); rows past nb
+    // are zero. Item (n, c, qc) covers columns 64 c + 8 qc .. +8 of sequence n.
+    constexpr int kUnroll = 4;
+#pragma unroll 1
+    for (int base = threadIdx.x; base < NP * 64; base += kThreads * kUnroll) {
+      float4 v[kUnroll][2];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int idx = base + u * kThreads;
+        const int n = idx >> 6;
+        if (idx < NP * 64 && n < nb) {
+          const float4* src = reinterpret_cast<const float4*>(o_lat + ((int64_t)(b0 + n) * n_h + h) * kLatent) +
+                              2 * (idx & 63);
+          v[u][0] = src[0];
+          v[u][1] = src[1];
+        } else {
+          v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int idx = base + u * kThreads;
+        if (idx >= NP * 64) continue;
+        const int n = idx >> 6, c = (idx >> 3) & 7, qc = idx & 7;
+        const float x[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+          const float2 hf = __bfloat1622float2(hv);
+          const __nv_bfloat162 lv = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+          hi[e] = *reinterpret_cast<const uint32_t*>(&hv);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&lv);
+        }
+        unsigned char* xs = smem + OFF_X + c * kXChunk;
+        const int rh = n, rl = NP + n;
+        *reinterpret_cast<uint4*>(xs + rh * 128 + ((qc ^ (rh & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(xs + rl * 128 + ((qc ^ (rl & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&bars[4]);
+    if (threadIdx.x == 0) {
+      const uint32_t idesc = idesc_f16(128, N, false, false, false);
+      bool ok = mbar_wait(&bars[4], 0, &never, kWaitNs);
+      for (int c = 0; ok && c < kChunks; ++c) {
+        if ((c & 1) == 0) ok = mbar_wait(&bars[c >> 1], 0, &never, kWaitNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t wt = smem_u32(smem + OFF_W + (c >> 1) * kWBox + (c & 1) * (kNope * 128));
+        const uint32_t xt = smem_u32(smem + OFF_X + c * kXChunk);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem, sdesc_sw128(wt + 32 * kk, 16, 1024), sdesc_sw128(xt + 32 * kk, 16, 1024), idesc,
+                 (c | kk) ? 1u : 0u);
+      }
+      if (!ok) *ok_word = 0;
+      mma_commit(&bars[5]);
+      // loads still in flight land before the CTA may leave
+      for (int i = 0; i < 4; ++i) mbar_wait(&bars[i], 0, &never, kWaitNs / 4);
+    }
+    __syncthreads();   // orders ok_word
+    // epilogue: lane d holds W_UV[h, d, :] · hi in column n and · lo in column NP + n
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bars[5], 0, &never, kWaitNs));
+    tc_fence_after();
+    if (done && *ok_word) {
+      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+      const int d = 32 * warp + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < NP; c0 += 16) {
+        uint32_t rh[16], rl[16];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                     : "=r"(rh[0]), "=r"(rh[1]), "=r"(rh[2]), "=r"(rh[3]), "=r"(rh[4]), "=r"(rh[5]), "=r"(rh[6]),
+                       "=r"(rh[7]), "=r"(rh[8]), "=r"(rh[9]), "=r"(rh[10]), "=r"(rh[11]), "=r"(rh[12]), "=r"(rh[13]),
+                       "=r"(rh[14]), "=r"(rh[15])
+                     : "r"(trow + c0));
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                     : "=r"(rl[0]), "=r"(rl[1]), "=r"(rl[2]), "=r"(rl[3]), "=r"(rl[4]), "=r"(rl[5]), "=r"(rl[6]),
+                       "=r"(rl[7]), "=r"(rl[8]), "=r"(rl[9]), "=r"(rl[10]), "=r"(rl[11]), "=r"(rl[12]), "=r"(rl[13]),
+                       "=r"(rl[14]), "=r"(rl[15])
+                     : "r"(trow + NP + c0));
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          if (c0 + x < nb)
+            o[((int64_t)(b0 + c0 + x) * n_h + h) * kNope + d] = __uint_as_float(rh[x]) + __uint_as_float(rl[x]);
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 64);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult qr;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
 }
 
 }  // namespace
 
 cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, int n_h, float* o,
                         cudaStream_t st) {
-  dim3 grid(n_h, ceil_div(B, kUpBT));
-  up_v_simt<<<grid, kUpWarps * 32, 0, st>>>(o_lat, w_uv, B, n_h, o);
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  // W_UV viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = 128 d rows x two chunks
+  CUtensorMap wmap;
+  cuuint64_t dims[3] = {64, (cuuint64_t)n_h * kNope, kChunks};
+  cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, 128};
+  cuuint32_t box[3] = {64, kNope, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (fn(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(w_uv), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(up_v_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  dim3 grid(n_h, ceil_div(B, kNB));
+  up_v_tc<<<grid, kThreads, kSmem, st>>>(wmap, o_lat, B, n_h, o);
   return cudaGetLastError();
 }
 
