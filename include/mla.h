@@ -173,6 +173,27 @@ MLA_API mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h
 MLA_API mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t* codes,
                             float* scales, cudaStream_t stream);
 
+/*
+ * mla_decode_combine_static — mla_decode_fwd followed by mla_combine with the split
+ * partials kept in a fixed device array inside the library instead of caller memory.
+ *   (No counterpart on the pages: it exists for callers that cannot allocate device
+ *   memory, e.g. an extension under a host framework that owns all of the GPU's memory,
+ *   or latency-critical code that cannot afford cudaMalloc's implicit synchronisation.)
+ *   Arguments as for mla_decode_fwd and mla_combine; o_lat [B, n_h, 512] fp32 out,
+ *   lse [B, n_h] fp32 out (may be NULL).
+ *   The partials need B * S * n_h * 2052 bytes (each of the two parts rounded up to
+ *   256 bytes); more than MLA_STATIC_SCRATCH_BYTES returns MLA_ERR_WORKSPACE before any
+ *   launch. The array (MLA_STATIC_SCRATCH_BYTES on every GPU that loads the library,
+ *   held until exit) is shared by all calls and keeps the last call's partials: calls
+ *   that overlap on the GPU race, and the caller must serialise them. The first call
+ *   on a device looks the array's device address up (cudaGetSymbolAddress) and should
+ *   come before any stream capture. Allocates nothing.
+ */
+#define MLA_STATIC_SCRATCH_BYTES (32 << 20)
+MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens,
+                                             int B, int n_h, int max_seq_len, float softmax_scale, int num_splits,
+                                             float* o_lat, float* lse, int32_t* status, cudaStream_t stream);
+
 /* Decode kernels (mla_decode_kernel's answer). */
 #define MLA_KERNEL_SIMT_F32 0   /* CUDA-core kernel, fp32 arithmetic                     */
 #define MLA_KERNEL_TC_BF16 1    /* tcgen05 tensor-core kernel, bf16 operands, fp32 accum.*/

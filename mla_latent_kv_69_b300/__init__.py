@@ -26,6 +26,7 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaEr
 
 __all__ = [
     "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range", "decode_kernel",
+    "decode_combine_static",
     "compute_dtype",
     "Cache", "MlaError", "status_string", "default_scale", "decode_step", "lib_path",
 ]
@@ -175,6 +176,26 @@ def combine(o_part, lse_part, o_lat=None, lse=None, stream=None):
     _need(lse, "lse", torch.float32, (B, n_h))
     check("mla_combine", _lib.get().mla_combine(_ptr(o_part), _ptr(lse_part), B, S, n_h, _ptr(o_lat), _ptr(lse),
                                               _stream(stream)))
+    return o_lat, lse
+
+
+def decode_combine_static(q_lat, cache: Cache, seq_lens, max_seq_len: int, o_lat, lse=None,
+                          softmax_scale: float | None = None, n_splits: int = 0, status=None, stream=None):
+    """decode_fwd + combine with the split partials in the library's fixed device array
+    (see mla_decode_combine_static in include/mla.h); the outputs are the caller's."""
+    B, n_h = q_lat.shape[0], q_lat.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, (B, n_h, D_ROW))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _need(o_lat, "o_lat", torch.float32, (B, n_h, D_LATENT))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, n_h))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    c = cache.to_c()
+    scale = default_scale() if softmax_scale is None else float(softmax_scale)
+    check("mla_decode_combine_static", _lib.get().mla_decode_combine_static(
+        _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale, int(n_splits),
+        _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
     return o_lat, lse
 
 

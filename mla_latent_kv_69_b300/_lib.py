@@ -21,10 +21,12 @@ MLA_ERR_DEVICE_BOUNDS = 6
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
 MLA_MAX_SPLITS = 256
+MLA_STATIC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
     "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version", "mla_decode_kernel",
+    "mla_decode_combine_static",
 ]
 
 
@@ -58,6 +60,8 @@ def _load():
     lib.mla_absorb_q.argtypes = [vp, vp, vp, i32, i32, f32, vp, vp]
     lib.mla_decode_fwd.argtypes = [vp, ctypes.POINTER(MlaCache), vp, i32, i32, i32, f32, i32, vp, vp, vp, vp]
     lib.mla_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.mla_decode_combine_static.argtypes = [vp, ctypes.POINTER(MlaCache), vp, i32, i32, i32, f32, i32, vp, vp, vp,
+                                              vp]
     lib.mla_up_v.argtypes = [vp, vp, i32, i32, vp, vp]
     lib.mla_quantize_fp8.argtypes = [vp, i64, vp, vp, vp]
     lib.mla_num_splits.argtypes = [i32, i32, i32]
@@ -66,7 +70,8 @@ def _load():
     lib.mla_status_string.argtypes = [i32]
     lib.mla_status_string.restype = ctypes.c_char_p
     for fn in ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
-               "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel"):
+               "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel",
+               "mla_decode_combine_static"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 

@@ -126,3 +126,12 @@ def test_other_calls_reject_bad_arguments_on_host():
     assert L.mla_quantize_fp8(A, -1, A, A, None) == INVALID
     assert L.mla_quantize_fp8(MIS, 10, A, A, None) == INVALID
     assert L.mla_quantize_fp8(A, 0, A, A, None) == _lib.MLA_OK      # nothing to do
+
+
+def test_static_entry_rejects_oversize_before_any_launch():
+    # 128 sequences x 256 splits x 128 heads of partials (~8.6 GB) exceed the fixed array
+    c = _cache(num_rows=128 * 4096)
+    rc = _lib.get().mla_decode_combine_static(A, ctypes.byref(c), A, 128, 128, 4096, 0.07, 256, A, A, None, None)
+    assert rc == _lib.MLA_ERR_WORKSPACE
+    assert _lib.get().mla_decode_combine_static(None, ctypes.byref(c), A, 32, 128, 4096, 0.07, 2, A, A, None,
+                                                None) == INVALID
