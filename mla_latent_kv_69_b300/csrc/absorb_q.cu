@@ -55,6 +55,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 48);
   volatile int* ok_word = reinterpret_cast<volatile int*>(smem + OFF_BAR + 52);
   const bool aligned = (smem_u32(smem) & 1023u) == 0;   // the 128B swizzle needs 1024-byte aligned tiles
+  griddep_launch_dependents();
 
   if (aligned) {
     if (threadIdx.x == 0) {
@@ -77,12 +78,13 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
       const uint64_t pol = l2_policy_evict_first();
       prefetch_tmap(&qmap);
       prefetch_tmap(&wmap);
-      mbar_arrive_expect_tx(&bars[4], 2 * kNB * 128);
-      tma_load_4d(smem + OFF_Q, &qmap, &bars[4], 0, h, b0, 0, pol);
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < 4; ++mt) {   // the weights do not depend on the previous kernel
         mbar_arrive_expect_tx(&bars[mt], kWTile);
         tma_load_3d(smem + OFF_W + mt * kWTile, &wmap, &bars[mt], 0, h * kNope, 2 * mt, pol);
       }
+      griddep_wait();
+      mbar_arrive_expect_tx(&bars[4], 2 * kNB * 128);
+      tma_load_4d(smem + OFF_Q, &qmap, &bars[4], 0, h, b0, 0, pol);
       const uint32_t idesc = idesc_f16(128, N, false, /*a_mn=*/true, /*b_mn=*/false);
       const volatile int never = 0;
       bool ok = mbar_wait(&bars[4], 0, &never, kWaitNs);
@@ -107,6 +109,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
       for (int mt = 0; mt < 4; ++mt) mbar_wait(&bars[mt], 0, &never, kWaitNs / 4);
     }
 
+    griddep_wait();   // q and pos may come from the previous kernel; q_lat may still be read by it
     // decoupled query, overlapping the tensor-core work: thread (n, g) rotates pairs
     // 8g .. 8g+7 of sequence n; every load of a pass is issued before any math
 #pragma unroll 1
@@ -171,6 +174,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
     }
     tc_fence_before();
   }
+  if (!aligned) griddep_wait();
   __syncthreads();
   tc_fence_after();
   if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 512);
@@ -230,8 +234,7 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, c
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(n_h, ceil_div(B, kNB));
-  absorb_q_tc<<<grid, kThreads, kSmem, st>>>(wmap, qmap, q, pos, B, n_h, turns, q_lat);
-  return cudaGetLastError();
+  return launch_overlapped(absorb_q_tc, grid, dim3(kThreads), kSmem, st, wmap, qmap, q, pos, B, n_h, turns, q_lat);
 }
 
 }  // namespace mla

@@ -18,6 +18,8 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
                float* __restrict__ o_lat, float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.x * kWarps + (threadIdx.x >> 5), b = blockIdx.y;
+  griddep_launch_dependents();
+  griddep_wait();   // the partials come from the previous kernel
   if (h >= n_h) return;
   const float* lp = lse_part + (int64_t)b * S * n_h + h;
   float m = -INFINITY;
@@ -78,8 +80,7 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int S, int n_h,
                            float* o_lat, float* lse, cudaStream_t st) {
   dim3 grid(ceil_div(n_h, kWarps), B);
-  combine_kernel<<<grid, kWarps * 32, 0, st>>>(o_part, lse_part, B, S, n_h, o_lat, lse);
-  return cudaGetLastError();
+  return launch_overlapped(combine_kernel, grid, dim3(kWarps * 32), 0, st, o_part, lse_part, B, S, n_h, o_lat, lse);
 }
 
 }  // namespace mla

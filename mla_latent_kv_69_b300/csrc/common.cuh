@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -83,5 +84,37 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t n, uint8_t* codes, float* scales,
                                 cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t st);
+
+}  // namespace mla
+
+namespace mla {
+
+// Programmatic dependent launch. Every kernel of the decode step lets the next one in
+// the stream start launching at its own entry (griddep_launch_dependents) and waits
+// for the previous kernel's completion and memory (griddep_wait) only before it reads
+// anything that kernel may write; each kernel waits before it finishes, so the order
+// stays transitive along the stream. Without a programmatic predecessor the wait
+// returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` so that it may overlap the tail of the previous kernel on `st`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace mla

@@ -186,8 +186,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
   split_range(L, p.S, s, &st, &en);
   const int n_tiles = (en - st + kTile - 1) / kTile;
   const int n_halves = 2 * n_tiles;
+  griddep_launch_dependents();
 
   if (n_tiles == 0) {   // empty split: nothing crosses the cluster
+    griddep_wait();
     if (rank == 1) {
       float* o = p.o_part + ((int64_t)b * p.S + s) * p.n_h * kLatent;
       for (int i = threadIdx.x; i < p.n_h * kLatent / 4; i += kThreads)
@@ -198,6 +200,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
     return;
   }
   if (smem_u32(smem) & 1023u) {   // the 128B swizzle needs 1024-byte aligned slots (same in both CTAs)
+    griddep_wait();
     if (threadIdx.x == 0) record_status(p.status, MLA_ERR_UNSUPPORTED);
     return;
   }
@@ -260,6 +263,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         prefetch_tmap(&smap);
         prefetch_tmap(&qmap);
         const int qrows = p.n_h < 128 ? p.n_h : 128;
+        griddep_wait();   // q_lat comes from the previous kernel
         mbar_arrive_expect_tx(&bars[SB_QFULL], 9 * qrows * 128);
         for (int g = 0; g < 3; ++g)
           tma_load_3d(smem + S_RING + g * kGroup, &qmap, &bars[SB_QFULL], 0, b * p.n_h, 3 * g, pol_first);
@@ -628,6 +632,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       }
       // epilogue: o_part = O / l, lse_part = (m + log2 l) · ln 2, staged in shared memory
       // (the c_KV stages are idle now) so that the global stores are coalesced rows
+      griddep_wait();   // o_part may still be read by the previous kernel of the stream
       const bool fin_ok = ok && warp_wait<true>(&bars[VB_FIN], 0, abort_flag);
       tc_fence_after();
       const float* fin = reinterpret_cast<const float*>(smem + V_PANEL);
@@ -748,8 +753,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   if (attr_err != cudaSuccess) return attr_err;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t ctas = 2ll * p.B * p.S;
-  decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(p, smap, vmap, qmap, omap, scale_log2);
-  return cudaGetLastError();
+  return launch_overlapped(decode_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmemBytes, st, p, smap, vmap,
+                           qmap, omap, scale_log2);
 }
 
 int decode_tc_num_splits(int B, int tiles, int n_h, int sms) {

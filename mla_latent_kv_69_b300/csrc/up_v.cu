@@ -46,6 +46,7 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 48);
   volatile int* ok_word = reinterpret_cast<volatile int*>(smem + OFF_BAR + 52);
   const bool aligned = (smem_u32(smem) & 1023u) == 0;   // the 128B swizzle needs 1024-byte aligned tiles
+  griddep_launch_dependents();
 
   if (aligned) {
     if (threadIdx.x == 0) {
@@ -75,6 +76,7 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
         tma_load_3d(smem + OFF_W + i * kWBox, &wmap, &bars[i], 0, h * kNope, 2 * i, pol);
       }
     }
+    griddep_wait();   // o_lat comes from the previous kernel
     // o_lat rows → bf16 hi/lo rows of every chunk (K-major, 128B swizzle); rows past nb
     // are zero. Item (n, c, qc) covers columns 64 c + 8 qc .. +8 of sequence n.
     constexpr int kUnroll = 4;
@@ -165,6 +167,7 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
     }
     tc_fence_before();
   }
+  if (!aligned) griddep_wait();
   __syncthreads();
   tc_fence_after();
   if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 64);
@@ -206,8 +209,7 @@ cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, in
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(n_h, ceil_div(B, kNB));
-  up_v_tc<<<grid, kThreads, kSmem, st>>>(wmap, o_lat, B, n_h, o);
-  return cudaGetLastError();
+  return launch_overlapped(up_v_tc, grid, dim3(kThreads), kSmem, st, wmap, o_lat, B, n_h, o);
 }
 
 }  // namespace mla
