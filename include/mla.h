@@ -197,6 +197,8 @@ MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache*
 /* Decode kernels (mla_decode_kernel's answer). */
 #define MLA_KERNEL_SIMT_F32 0   /* CUDA-core kernel, fp32 arithmetic                     */
 #define MLA_KERNEL_TC_BF16 1    /* tcgen05 tensor-core kernel, bf16 operands, fp32 accum.*/
+#define MLA_KERNEL_TC_F16_E4M3 2 /* tcgen05 kernel for an e4m3 cache: codes converted to f16
+                                   exactly, query rounded to f16, fp32 accumulation      */
 
 /* Which decode kernel mla_decode_fwd runs for this cache dtype and head count
  * (-1 for an invalid combination). Host only. */

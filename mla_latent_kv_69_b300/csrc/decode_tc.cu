@@ -61,7 +61,7 @@ constexpr int kPanel = 128 * 128;          // P for 64 tokens: 128 heads x 64 bf
 constexpr int kHdr = 512 + 16;             // 128 fp32 rescale factors and a flag word (with panel 0)
 constexpr int kFinBytes = 128 * 2 * 4;     // final (m, l) per head
 constexpr int kThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2..9 row warps
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kWaitNs = kDecodeWaitNs;
 constexpr float kRescaleLog2 = 8.f;
 
 constexpr uint32_t kQCol = 0;              // score CTA TMEM: Q as bf16 pairs (288 columns)
@@ -107,52 +107,6 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(S_PANEL % 1024 == 0 && V_PANEL % 1024 == 0 && kGroup % 1024 == 0, "swizzle alignment");
 
 enum Cmd { CMD_ZERO = 1, CMD_RESCALE = 2, CMD_DONE = 4 };
-
-// 64-token half u of the split [st, en) of sequence b.
-struct HalfInfo {
-  int row0;     // first cache row (the TMA y coordinate)
-  int nvalid;   // tokens of the half that belong to the split
-  bool load;    // some token is valid and its rows lie inside the caller's buffers
-};
-
-__device__ __forceinline__ HalfInfo half_info(const DecodeParams& p, int b, int st, int en, int u, bool record) {
-  HalfInfo hi;
-  const int t0 = st + kHalf * u;
-  hi.nvalid = max(0, min(kHalf, en - t0));
-  hi.row0 = 0;
-  hi.load = hi.nvalid > 0;
-  if (!hi.load) return hi;
-  bool valid = true;
-  if (p.block_table) {
-    const int pi = t0 >> 6;
-    const int page = pi < p.max_pages ? p.block_table[(int64_t)b * p.max_pages + pi] : -1;
-    if (page < 0 || (int64_t)page * kHalf >= p.num_rows) valid = false;
-    else hi.row0 = page * kHalf;
-  } else {
-    const int64_t row = (int64_t)b * p.seq_stride + t0;
-    if (t0 >= p.seq_stride || row >= p.num_rows) {
-      valid = false;
-    } else {
-      hi.row0 = (int)row;
-      const int64_t room = (p.seq_stride - t0) < (p.num_rows - row) ? (p.seq_stride - t0) : (p.num_rows - row);
-      if (room < hi.nvalid) hi.nvalid = (int)room;
-    }
-  }
-  if (!valid) {
-    if (record) record_status(p.status, MLA_ERR_DEVICE_BOUNDS);
-    hi.nvalid = 0;
-    hi.load = false;
-  }
-  return hi;
-}
-
-// A bounded wait taken by all 32 lanes of a warp together: every lane returns the same
-// answer, so warp-collective code after it never runs with lanes missing.
-template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
-  const bool ok = mbar_wait<kCluster>(bar, parity, abort_flag, kWaitNs);
-  return __all_sync(0xffffffffu, ok);
-}
 
 __device__ __forceinline__ void give_up(const DecodeParams& p, volatile int* abort_flag, unsigned char* smem,
                                         uint32_t peer) {
@@ -731,7 +685,8 @@ bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
 }  // namespace
 
 bool decode_tc_supported(const DecodeParams& p) {
-  return p.kv_dtype == MLA_KV_BF16 && p.num_rows >= 1 && p.num_rows < (int64_t)INT_MAX - 2 * kTile;
+  return (p.kv_dtype == MLA_KV_BF16 || p.kv_dtype == MLA_KV_FP8_E4M3) && p.num_rows >= 1 &&
+         p.num_rows < (int64_t)INT_MAX - 2 * kTile;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_t st) {

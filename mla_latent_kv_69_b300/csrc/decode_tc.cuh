@@ -1,11 +1,63 @@
 // Tensor-core (tcgen05 + TMEM + TMA) split-KV decode: host-side entry points.
 #pragma once
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 
-// True when the tcgen05 kernel handles this configuration.
+constexpr uint64_t kDecodeWaitNs = 2000000000ull;   // every mbarrier wait of the decode kernels
+constexpr int kDecodeHalf = 64;                     // tokens per value step (= one page)
+
+// 64-token half u of the split [st, en) of sequence b.
+struct HalfInfo {
+  int row0;     // first cache row (the TMA y coordinate)
+  int nvalid;   // tokens of the half that belong to the split
+  bool load;    // some token is valid and its rows lie inside the caller's buffers
+};
+
+__device__ __forceinline__ HalfInfo half_info(const DecodeParams& p, int b, int st, int en, int u, bool record) {
+  HalfInfo hi;
+  const int t0 = st + kDecodeHalf * u;
+  hi.nvalid = max(0, min(kDecodeHalf, en - t0));
+  hi.row0 = 0;
+  hi.load = hi.nvalid > 0;
+  if (!hi.load) return hi;
+  bool valid = true;
+  if (p.block_table) {
+    const int pi = t0 >> 6;
+    const int page = pi < p.max_pages ? p.block_table[(int64_t)b * p.max_pages + pi] : -1;
+    if (page < 0 || (int64_t)page * kDecodeHalf >= p.num_rows) valid = false;
+    else hi.row0 = page * kDecodeHalf;
+  } else {
+    const int64_t row = (int64_t)b * p.seq_stride + t0;
+    if (t0 >= p.seq_stride || row >= p.num_rows) {
+      valid = false;
+    } else {
+      hi.row0 = (int)row;
+      const int64_t room = (p.seq_stride - t0) < (p.num_rows - row) ? (p.seq_stride - t0) : (p.num_rows - row);
+      if (room < hi.nvalid) hi.nvalid = (int)room;
+    }
+  }
+  if (!valid) {
+    if (record) record_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+    hi.nvalid = 0;
+    hi.load = false;
+  }
+  return hi;
+}
+
+// A bounded wait taken by all 32 lanes of a warp together: every lane returns the same
+// answer, so warp-collective code after it never runs with lanes missing.
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+  const bool ok = sm100::mbar_wait<kCluster>(bar, parity, abort_flag, kDecodeWaitNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// True when the tcgen05 kernels handle this configuration.
 bool decode_tc_supported(const DecodeParams& p);
+// e4m3 cache: tcgen05 kernel with f16 operands (decode_tc_fp8.cu).
+cudaError_t launch_decode_tc_fp8(const DecodeParams& p, cudaStream_t st);
 // Launch; max_seq_len sizes nothing on the device side but is kept for heuristics.
 cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_t st);
 // Split count for B sequences of up to `tiles` 64-token tiles.

@@ -72,7 +72,8 @@ int mla_decode_kernel(int kv_dtype, int n_h) {
   p.kv_dtype = kv_dtype;
   p.n_h = n_h;
   p.num_rows = 1;
-  return decode_tc_supported(p) ? MLA_KERNEL_TC_BF16 : MLA_KERNEL_SIMT_F32;
+  if (!decode_tc_supported(p)) return MLA_KERNEL_SIMT_F32;
+  return kv_dtype == MLA_KV_BF16 ? MLA_KERNEL_TC_BF16 : MLA_KERNEL_TC_F16_E4M3;
 }
 
 int mla_num_splits(int B, int max_seq_len, int n_h) {
@@ -144,7 +145,9 @@ mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32
   p.n_h = n_h;
   p.S = S;
   p.scale = softmax_scale;
-  if (decode_tc_supported(p)) return cuda_status(launch_decode_tc(p, max_seq_len, stream));
+  if (decode_tc_supported(p))
+    return cuda_status(p.kv_dtype == MLA_KV_BF16 ? launch_decode_tc(p, max_seq_len, stream)
+                                                 : launch_decode_tc_fp8(p, stream));
   return cuda_status(launch_decode_simt(p, stream));
 }
 

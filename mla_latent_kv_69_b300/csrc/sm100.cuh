@@ -398,3 +398,13 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 }
 }  // namespace sm100
 }  // namespace mla
+
+namespace mla {
+namespace sm100 {
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+}  // namespace sm100
+}  // namespace mla

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import mla_latent_kv_69_b300 as mla
 import workloads as W
 from mla_cases import Case, assert_within_tolerance, rows_f32
 from oracle import fp8_e4m3
@@ -96,6 +97,44 @@ def test_fp8_quantiser_bit_exact_small(cuda_device):
             case = Case(w, cuda_device, lens=lens, keep_rows=True)
             for b in range(case.B):
                 _fp8_codes_match(case, b)
+
+
+class _CodesCase(Case):
+    """An e4m3 case whose codes and per-token scales are drawn on the host and written
+    into the device cache directly; the oracle decodes the same codes."""
+
+    def set_codes(self, b, codes, scales):
+        L = len(codes)
+        self.cache.data[b, :L] = torch.from_numpy(codes).to(self.device)
+        self.cache.scales[b, :L] = torch.from_numpy(scales).to(self.device)
+        self.host_codes = getattr(self, "host_codes", {})
+        self.host_codes[b] = (codes, scales)
+
+    def oracle_rows(self, b):
+        codes, scales = self.host_codes[b]
+        return fp8_e4m3.dequantize_rows(codes, scales)
+
+
+def test_fp8_every_code_through_tensor_cores(cuda_device):
+    """Every finite e4m3 code, half of them drawn from the subnormal codes (exponent field
+    0), through both contractions of the e4m3 kernel: the code-to-f16 mapping has to be
+    exact for normal and subnormal codes alike for the result to stay in tolerance."""
+    w = W.Workload("codes", n_h=128, batch=2, ctx=0, kv="fp8", seed=21)
+    case = _CodesCase(w, cuda_device, lens=[300, 257])
+    rng = np.random.default_rng(2101)
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    sub = finite[((finite >> 3) & 15) == 0]
+    for b, L in enumerate(case.lens):
+        L = int(L)
+        codes = np.where(rng.random((L, 576)) < 0.5, rng.choice(sub, (L, 576)), rng.choice(finite, (L, 576)))
+        scales = (rng.uniform(0.5, 1.0, L) / 448.0).astype(np.float32)
+        case.set_codes(b, codes.astype(np.uint8), scales)
+    assert mla.decode_kernel("fp8", 128) == "tcgen05_f16_e4m3"
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    out = case.run(n_splits=3, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _compare(case, out, [(b, None) for b in range(case.B)])
 
 
 FULL = {
