@@ -594,38 +594,43 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       const float l = fin[2 * h + 1];
       const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
       const float inv = good ? 1.f / l : 0.f;
-      // Two passes of 256 columns; each pass is 8 chunks of 32 fp32, staged chunk-major
-      // and 128B-swizzled ([chunk][head][32]) and written by one 3D TMA store.
+      // Each row warp owns 32 heads x 256 columns: eight 32-column chunks, each scaled,
+      // staged 128B-swizzled in a 4 KB buffer of the warp's own and written at once by a
+      // TMA store that the warp issues; four buffers per warp rotate, so the stores
+      // overlap the TMEM reads of the next chunks.
       const int rows = p.n_h < 128 ? p.n_h : 128;
-      unsigned char* stg = smem + V_CST;
-      const int orow0 = (b * p.S + s) * p.n_h;
+      const int wrows = rows < 32 ? rows : 32;
+      const bool wlive = 32 * q < rows;
+      unsigned char* wst = smem + V_CST + (warp - 2) * 16384;
+      const int orow0 = (b * p.S + s) * p.n_h + 32 * q;
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
+      for (int cc = 0; cc < 8; ++cc) {
+        const int chunk = 8 * j + cc;
         uint32_t r[32];
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int chunk = 4 * j + cc;
-          MLA_TMEM_LD32(trow + kOCol + 256 * pass + 32 * chunk, r);
-          tmem_wait_ld();
-          if (h < rows) {
-            unsigned char* dst = stg + chunk * (rows * 128) + h * 128;
+        MLA_TMEM_LD32(trow + kOCol + 32 * chunk, r);
+        tmem_wait_ld();
+        if (!wlive) continue;
+        unsigned char* buf = wst + (cc & 3) * 4096;
+        if (cc >= 4) {   // this buffer's previous store has to have read it
+          if (lane == 0) bulk_wait_group_read<3>();
+          __syncwarp();
+        }
+        if (lane < wrows) {
+          unsigned char* dst = buf + lane * 128;
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              *reinterpret_cast<float4*>(dst + ((x ^ (h & 7)) << 4)) =
-                  make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
-                              __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
-          }
+          for (int x = 0; x < 8; ++x)
+            *reinterpret_cast<float4*>(dst + ((x ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
+                            __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
         }
         fence_proxy_async_smem();
-        named_sync(1, 256);
-        if (tid == 0) {
-          tma_store_3d(&omap, stg, 0, orow0, 8 * pass);
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&omap, buf, 0, orow0, chunk);
           bulk_commit_group();
-          bulk_wait_group_read0();   // the staging area is reused by the next pass
         }
-        named_sync(1, 256);
       }
-      if (tid == 0) bulk_wait_group0();
+      if (wlive && lane == 0) bulk_wait_group0();
       if (j == 0 && h < p.n_h)
         p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] =
             good ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -669,13 +674,13 @@ bool make_row_map(const void* base, int64_t rows, int box_rows, int box_chunks, 
 }
 
 // 3D map over the fp32 partial results [rows][512] seen as (32 values, row, 16 chunks of
-// 32), 128B swizzle; a box of `box_rows` rows x 8 chunks is one 256-column half.
+// 32), 128B swizzle; a box is `box_rows` rows (32, or n_h when smaller) x one chunk.
 bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)(kLatent / 32)};
   cuuint64_t strides[2] = {(cuuint64_t)kLatent * 4, 128};
-  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 8};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
@@ -698,7 +703,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   if (!make_row_map(p.data, p.num_rows, p.block_table ? 64 : kTile, p.block_table ? 1 : 3, &smap) ||
       !make_row_map(p.data, p.num_rows, 64, 8, &vmap) ||
       !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap) ||
-      !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 128 ? p.n_h : 128, &omap))
+      !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 32 ? p.n_h : 32, &omap))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

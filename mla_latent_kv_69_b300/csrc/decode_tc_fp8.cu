@@ -611,7 +611,6 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       const int q = warp & 3;
       const int h = q * 32 + lane;
       const int j = (warp - 2) >> 2;
-      const int tid = threadIdx.x - 64;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
       int k = 0;
       bool ok = true;
@@ -652,36 +651,43 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       const float l = fin[2 * h + 1];
       const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
       const float inv = good ? 256.f / l : 0.f;   // 2^8 undoes the operand scaling
+      // Each row warp owns 32 heads x 256 columns: eight 32-column chunks, each scaled,
+      // staged 128B-swizzled in a 4 KB buffer of the warp's own and written at once by a
+      // TMA store that the warp issues; four buffers per warp rotate, so the stores
+      // overlap the TMEM reads of the next chunks.
       const int rows = p.n_h < 128 ? p.n_h : 128;
-      unsigned char* stg = smem + V_F16;
-      const int orow0 = (b * p.S + s) * p.n_h;
+      const int wrows = rows < 32 ? rows : 32;
+      const bool wlive = 32 * q < rows;
+      unsigned char* wst = smem + V_F16 + (warp - 2) * 16384;
+      const int orow0 = (b * p.S + s) * p.n_h + 32 * q;
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        uint32_t rg[32];
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int chunk = 4 * j + cc;
-          MLA_TMEM_LD32(trow + kOCol + 256 * pass + 32 * chunk, rg);
-          tmem_wait_ld();
-          if (h < rows) {
-            unsigned char* dst = stg + chunk * (rows * 128) + h * 128;
+      for (int cc = 0; cc < 8; ++cc) {
+        const int chunk = 8 * j + cc;
+        uint32_t r[32];
+        MLA_TMEM_LD32(trow + kOCol + 32 * chunk, r);
+        tmem_wait_ld();
+        if (!wlive) continue;
+        unsigned char* buf = wst + (cc & 3) * 4096;
+        if (cc >= 4) {   // this buffer's previous store has to have read it
+          if (lane == 0) bulk_wait_group_read<3>();
+          __syncwarp();
+        }
+        if (lane < wrows) {
+          unsigned char* dst = buf + lane * 128;
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              *reinterpret_cast<float4*>(dst + ((x ^ (h & 7)) << 4)) =
-                  make_float4(__uint_as_float(rg[4 * x]) * inv, __uint_as_float(rg[4 * x + 1]) * inv,
-                              __uint_as_float(rg[4 * x + 2]) * inv, __uint_as_float(rg[4 * x + 3]) * inv);
-          }
+          for (int x = 0; x < 8; ++x)
+            *reinterpret_cast<float4*>(dst + ((x ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
+                            __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
         }
         fence_proxy_async_smem();
-        named_sync(1, 256);
-        if (tid == 0) {
-          tma_store_3d(&omap, stg, 0, orow0, 8 * pass);
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&omap, buf, 0, orow0, chunk);
           bulk_commit_group();
-          bulk_wait_group_read0();
         }
-        named_sync(1, 256);
       }
-      if (tid == 0) bulk_wait_group0();
+      if (wlive && lane == 0) bulk_wait_group0();
       if (j == 0 && h < p.n_h)
         p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] =
             good ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -734,12 +740,14 @@ bool make_q_map(const void* base, int64_t rows, int box_rows, CUtensorMap* map) 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 partial results [rows][512] as (32 values, row, 16 chunks of 32), 128B swizzle;
+// a box is `box_rows` rows x one chunk (one row warp's store).
 bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)(kLatent / 32)};
   cuuint64_t strides[2] = {(cuuint64_t)kLatent * 4, 128};
-  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 8};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
@@ -753,7 +761,7 @@ cudaError_t launch_decode_tc_fp8(const DecodeParams& p, cudaStream_t st) {
   CUtensorMap e4s, e4v, qmap, omap;
   if (!make_code_map(p.data, p.num_rows, 64, 3, &e4s) || !make_code_map(p.data, p.num_rows, 64, 8, &e4v) ||
       !make_q_map(p.q_lat, (int64_t)p.B * p.n_h, rows, &qmap) ||
-      !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, rows, &omap))
+      !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 32 ? p.n_h : 32, &omap))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
