@@ -8,8 +8,9 @@
 //
 // A kind::f16 MMA takes two operands of one type and an 8-bit query would not keep the
 // error budget, so both contractions run on f16 operands: every e4m3 code maps to the f16
-// of 2^-8 times its value, which is exact (see e4m3x16_to_f16), and the query is rounded
-// from bf16 to f16 (10 significant bits against bf16's 8). The 2^8 comes back in fp32:
+// of 2^-8 times its value, which is exact (see e4m3x16_to_f16), and the query converts
+// from bf16 to f16 exactly within f16's range (11 significant bits against bf16's 8).
+// The 2^8 comes back in fp32:
 // in the score scale and in the output's 1/l. Each CTA has four converter warps that
 // turn TMA-loaded e4m3 rows into 128B-swizzled f16 operand tiles:
 //   score CTA  e4m3 ring of five 24 KB groups (128 tokens x 3 column chunks) →
@@ -72,8 +73,8 @@ constexpr int V_END = V_HDR + 1024;
 constexpr int OFF_BAR = (S_END > V_END ? S_END : V_END);
 enum Bar {
   SB_E4FULL = 0,                          // [kE4Ring] e4m3 group landed
-  SB_E4EMPTY = SB_E4FULL + kE4Ring,       // [kE4Ring] converters done with it (128)
-  SB_F16FULL = SB_E4EMPTY + kE4Ring,      // [kF16Ring] f16 slot written (128)
+  SB_E4EMPTY = SB_E4FULL + kE4Ring,       // [kE4Ring] converters done with it (4 warps)
+  SB_F16FULL = SB_E4EMPTY + kE4Ring,      // [kF16Ring] f16 slot written (4 warps)
   SB_F16EMPTY = SB_F16FULL + kF16Ring,    // [kF16Ring] QK MMAs done with it
   SB_QFULL = SB_F16EMPTY + kF16Ring,
   SB_QREADY = SB_QFULL + 1,               // (256)
@@ -84,8 +85,8 @@ enum Bar {
   SB_SCLREADY = SB_FLUSH + 1,             // [2] tile scales stored (128)
   SB_SCLFREE = SB_SCLREADY + 2,           // [2] tile scales read (256)
   VB_E4FULL = SB_SCLFREE + 2,             // [2]
-  VB_E4EMPTY = VB_E4FULL + 2,             // [2] (128)
-  VB_F16FULL = VB_E4EMPTY + 2,            // [2] (128)
+  VB_E4EMPTY = VB_E4FULL + 2,             // [2] (4 warps)
+  VB_F16FULL = VB_E4EMPTY + 2,            // [2] (4 warps)
   VB_F16EMPTY = VB_F16FULL + 2,           // [2] PV MMAs done with the stage
   VB_PFULL = VB_F16EMPTY + 2,             // [2]
   VB_FIN = VB_PFULL + 2,
@@ -133,17 +134,17 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// Converts one 64-code row segment at `src` into the 128-byte swizzled f16 row at
-// `dst_row` (row index `r` selects the swizzle phase); zero when `valid` is false.
-__device__ __forceinline__ void convert_row64(const unsigned char* src, unsigned char* dst_row, int r, bool valid) {
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    const int q = (q4 + r) & 3;   // staggered order spreads the 64-byte-stride reads over banks
-    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-    if (valid) e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src + 16 * q), lo, hi);
-    *reinterpret_cast<uint4*>(dst_row + (((2 * q) ^ (r & 7)) << 4)) = lo;
-    *reinterpret_cast<uint4*>(dst_row + (((2 * q + 1) ^ (r & 7)) << 4)) = hi;
-  }
+// Converts the 16 codes at `src` (columns 16 c16 .. 16 c16 + 15 of an e4m3 row) into
+// 16-byte units 2 c16 and 2 c16 + 1 of the 128B-swizzled f16 row `row` at `dst_row`;
+// zero when `valid` is false. The converters hand out units so that a warp reads 512
+// contiguous bytes (eight 64-byte rows) per load and its stores hit each bank group
+// four times: both are conflict-free.
+__device__ __forceinline__ void convert_unit(const unsigned char* src, unsigned char* dst_row, int row, int c16,
+                                             bool valid) {
+  uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+  if (valid) e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src), lo, hi);
+  *reinterpret_cast<uint4*>(dst_row + (((2 * c16) ^ (row & 7)) << 4)) = lo;
+  *reinterpret_cast<uint4*>(dst_row + (((2 * c16 + 1) ^ (row & 7)) << 4)) = hi;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -191,10 +192,10 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
     *o_init_word = 0;
     for (int k = 0; k < kE4Ring; ++k) {
       mbar_init(&bars[SB_E4FULL + k], 1);
-      mbar_init(&bars[SB_E4EMPTY + k], 128);
+      mbar_init(&bars[SB_E4EMPTY + k], 4);
     }
     for (int k = 0; k < kF16Ring; ++k) {
-      mbar_init(&bars[SB_F16FULL + k], 128);
+      mbar_init(&bars[SB_F16FULL + k], 4);
       mbar_init(&bars[SB_F16EMPTY + k], 1);
     }
     mbar_init(&bars[SB_QFULL], 1);
@@ -206,8 +207,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       mbar_init(&bars[SB_SCLREADY + k], 128);
       mbar_init(&bars[SB_SCLFREE + k], 256);
       mbar_init(&bars[VB_E4FULL + k], 1);
-      mbar_init(&bars[VB_E4EMPTY + k], 128);
-      mbar_init(&bars[VB_F16FULL + k], 128);
+      mbar_init(&bars[VB_E4EMPTY + k], 4);
+      mbar_init(&bars[VB_F16FULL + k], 4);
       mbar_init(&bars[VB_F16EMPTY + k], 1);
       mbar_init(&bars[VB_PFULL + k], 1);
     }
@@ -318,11 +319,12 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       const int r = ct, hh = r >> 6, rr = r & 63;
       float* scl = reinterpret_cast<float*>(smem + S_SCL);
       bool ok = true;
-      // this row's scale, loaded one tile ahead so that its latency stays off the path
+      // this row's scale, loaded one tile ahead by a predicated load (no select on the
+      // loaded value), so that nothing waits for it before the next tile stores it
       auto row_scale = [&](int tile) -> float {
         if (tile >= n_tiles) return 0.f;
         const HalfInfo hi = half_info(p, b, st, en, 2 * tile + hh, false);
-        return (hi.load && rr < hi.nvalid) ? p.scales[hi.row0 + rr] : 0.f;
+        return ld_global_nc_or_zero(p.scales + hi.row0 + rr, hi.load && rr < hi.nvalid);
       };
       float sc_next = row_scale(0);
       for (int i = 0; i < n_tiles && ok; ++i) {
@@ -336,19 +338,29 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         for (int c = 0; c < 9; ++c) {
           const int k = 3 * i + c / 3, e = k % kE4Ring;
           const int fi = 9 * i + c, f = fi % kF16Ring;
-          if (c % 3 == 0 && !mbar_wait(&bars[SB_E4FULL + e], (k / kE4Ring) & 1, abort_flag, kWaitNs)) {
+          if (c % 3 == 0 && !warp_wait(&bars[SB_E4FULL + e], (k / kE4Ring) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          if (fi >= kF16Ring && !mbar_wait(&bars[SB_F16EMPTY + f], ((fi / kF16Ring) - 1) & 1, abort_flag, kWaitNs)) {
+          if (fi >= kF16Ring && !warp_wait(&bars[SB_F16EMPTY + f], ((fi / kF16Ring) - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          const unsigned char* src = smem + S_E4 + e * kE4Group + hh * (kE4Group / 2) + (c % 3) * 4096 + rr * 64;
-          convert_row64(src, smem + S_F16 + f * kF16Slot + r * 128, r, true);
+          // 128 rows x 64 codes: unit u = 128 k + ct is row u / 4, codes 16 (u % 4) ..
+          const unsigned char* gsrc = smem + S_E4 + e * kE4Group + (c % 3) * 4096;
+          unsigned char* slot = smem + S_F16 + f * kF16Slot;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int u = 128 * kk + ct, row = u >> 2, c16 = u & 3;
+            convert_unit(gsrc + (row >> 6) * (kE4Group / 2) + (row & 63) * 64 + 16 * c16, slot + row * 128, row, c16,
+                         true);
+          }
           fence_proxy_async_smem();
-          mbar_arrive(&bars[SB_F16FULL + f]);
-          if (c % 3 == 2) mbar_arrive(&bars[SB_E4EMPTY + e]);
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars[SB_F16FULL + f]);
+            if (c % 3 == 2) mbar_arrive(&bars[SB_E4EMPTY + e]);
+          }
         }
       }
       if (!ok) give_up(p, abort_flag, smem, peer);
@@ -447,6 +459,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         // within the register budget of a 14-warp CTA.
         if (i > 0) mbar_wait<true>(&bars[SB_PFREE + j], (i - 1) & 1, abort_flag, kWaitNs);
         unsigned char* stg = smem + S_PANEL + j * kPanel;
+        unsigned char* hdr = smem + S_HDR;
         float lsum = 0.f;
         const bool live = m_run != -INFINITY;
         const float2 nm2 = make_float2(live ? -m_run : 0.f, live ? -m_run : 0.f);
@@ -473,14 +486,14 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         l_run += lsum;
         mbar_arrive(&bars[SB_SCLFREE + (i & 1)]);
         if (j == 0) {
-          reinterpret_cast<float*>(smem + S_HDR)[h] = fac;
-          if (h == 0) reinterpret_cast<uint32_t*>(smem + S_HDR + 512)[0] = nres;
+          reinterpret_cast<float*>(hdr)[h] = fac;
+          if (h == 0) reinterpret_cast<uint32_t*>(hdr + 512)[0] = nres;
         }
         fence_proxy_async_smem();
         named_sync(2 + j, 128);
         if (q == 0 && lane == 0 && !*abort_flag) {
           bulk_copy_to_peer(panel_remote, stg, kPanel, pfull_remote);
-          if (j == 0) bulk_copy_to_peer(hdr_remote, smem + S_HDR, kHdr, pfull_remote);
+          if (j == 0) bulk_copy_to_peer(hdr_remote, hdr, kHdr, pfull_remote);
         }
       }
       named_sync(1, 256);
@@ -584,26 +597,30 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
     } else if (warp >= 10) {
       // ---- converters: e4m3 step → f16 stage; rows past the split become zero ----
       const int ct = threadIdx.x - kConvBase;
-      const int r = ct & 63, cg = ct >> 6;   // row, chunk group (chunks 4 cg .. 4 cg + 3)
       bool ok = true;
       for (int u = 0; u < n_halves && ok; ++u) {
         const int e = u & 1, sg = u & 1;
-        if (!mbar_wait(&bars[VB_E4FULL + e], (u >> 1) & 1, abort_flag, kWaitNs) ||
-            (u >= 2 && !mbar_wait(&bars[VB_F16EMPTY + sg], ((u >> 1) - 1) & 1, abort_flag, kWaitNs))) {
+        if (!warp_wait(&bars[VB_E4FULL + e], (u >> 1) & 1, abort_flag) ||
+            (u >= 2 && !warp_wait(&bars[VB_F16EMPTY + sg], ((u >> 1) - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         const HalfInfo hi = half_info(p, b, st, en, u, false);
-        const bool valid = hi.load && r < hi.nvalid;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = 4 * cg + cc;
-          convert_row64(smem + V_E4 + e * kVE4 + c * 4096 + r * 64, smem + V_F16 + sg * kVStage + c * 8192 + r * 128,
-                        r, valid);
+        const unsigned char* vsrc = smem + V_E4 + e * kVE4;
+        unsigned char* vdst = smem + V_F16 + sg * kVStage;
+        // 8 chunks x 64 rows x 64 codes: unit f = 128 k + ct is chunk f / 256, row (f % 256) / 4
+#pragma unroll 4
+        for (int kk = 0; kk < 16; ++kk) {
+          const int f = 128 * kk + ct, chunk = f >> 8, row = (f & 255) >> 2, c16 = f & 3;
+          convert_unit(vsrc + chunk * 4096 + row * 64 + 16 * c16, vdst + chunk * 8192 + row * 128, row, c16,
+                       hi.load && row < hi.nvalid);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars[VB_F16FULL + sg]);
-        mbar_arrive(&bars[VB_E4EMPTY + e]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[VB_F16FULL + sg]);
+          mbar_arrive(&bars[VB_E4EMPTY + e]);
+        }
       }
       if (!ok) give_up(p, abort_flag, smem, peer);
     } else {

@@ -98,6 +98,33 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// The same probes with a suspend-time hint: a thread whose phase is not complete yet may
+// sleep up to `hint_ns` and is woken when the phase completes, so waiting warps stop
+// taking issue slots from the warps that share their scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSleepHintNs = 20000;   // a sleeping waiter still re-checks abort and time
+
 // Bounded wait: true once the phase with `parity` completed; false after `limit_ns`
 // or as soon as *abort becomes non-zero (another role gave up).
 template <bool kCluster = false>
@@ -105,14 +132,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
                                           uint64_t limit_ns) {
   auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (probe()) return true;
+  auto sleep_probe = [&]() {
+    return kCluster ? mbar_try_wait_cluster_sleep(bar, parity, kSleepHintNs)
+                    : mbar_try_wait_sleep(bar, parity, kSleepHintNs);
+  };
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (probe()) return true;
+      if (sleep_probe()) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Read-only global load of one float under a predicate; 0 when `pred` is false. The
+// result register is written by the load itself, so the thread stalls only where the
+// value is first used.
+__device__ __forceinline__ float ld_global_nc_or_zero(const float* ptr, bool pred) {
+  float v;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %2, 0;\n\t"
+      "mov.b32 %0, 0;\n\t"
+      "@q ld.global.nc.f32 %0, [%1];\n\t}"
+      : "=f"(v)
+      : "l"(ptr), "r"((int)pred));
+  return v;
 }
 
 // ------------------------------------ TMA -------------------------------------------
