@@ -132,6 +132,7 @@ MLA_API mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* 
  *              (-inf, with o_part = 0, for a split that holds no token)
  *   status     optional device int32 (may be NULL)
  *   Split s of sequence b covers the tokens mla_split_range(L_b, S, s) returns.
+ *   A cache of 2^31 - 256 rows or more returns MLA_ERR_UNSUPPORTED (32-bit TMA rows).
  */
 MLA_API mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache,
                           const int32_t* seq_lens, int B, int n_h, int max_seq_len,
@@ -195,10 +196,10 @@ MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache*
                                              float* o_lat, float* lse, int32_t* status, cudaStream_t stream);
 
 /* Decode kernels (mla_decode_kernel's answer). */
-#define MLA_KERNEL_SIMT_F32 0   /* CUDA-core kernel, fp32 arithmetic                     */
 #define MLA_KERNEL_TC_BF16 1    /* tcgen05 tensor-core kernel, bf16 operands, fp32 accum.*/
 #define MLA_KERNEL_TC_F16_E4M3 2 /* tcgen05 kernel for an e4m3 cache: codes converted to f16
-                                   exactly, query rounded to f16, fp32 accumulation      */
+                                   exactly (as 2^-8 x value), query converted to f16,
+                                   fp32 accumulation                                     */
 
 /* Which decode kernel mla_decode_fwd runs for this cache dtype and head count
  * (-1 for an invalid combination). Host only. */

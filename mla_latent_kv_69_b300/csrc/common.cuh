@@ -83,7 +83,6 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
                            float* o_lat, float* lse, cudaStream_t st);
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t n, uint8_t* codes, float* scales,
                                 cudaStream_t st);
-cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t st);
 
 }  // namespace mla
 

@@ -72,7 +72,7 @@ int mla_decode_kernel(int kv_dtype, int n_h) {
   p.kv_dtype = kv_dtype;
   p.n_h = n_h;
   p.num_rows = 1;
-  if (!decode_tc_supported(p)) return MLA_KERNEL_SIMT_F32;
+  if (!decode_tc_supported(p)) return -1;
   return kv_dtype == MLA_KV_BF16 ? MLA_KERNEL_TC_BF16 : MLA_KERNEL_TC_F16_E4M3;
 }
 
@@ -145,10 +145,10 @@ mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32
   p.n_h = n_h;
   p.S = S;
   p.scale = softmax_scale;
-  if (decode_tc_supported(p))
-    return cuda_status(p.kv_dtype == MLA_KV_BF16 ? launch_decode_tc(p, max_seq_len, stream)
-                                                 : launch_decode_tc_fp8(p, stream));
-  return cuda_status(launch_decode_simt(p, stream));
+  // TMA coordinates are 32-bit: a cache of 2^31 rows (over 1 TB) is not served.
+  if (!decode_tc_supported(p)) return MLA_ERR_UNSUPPORTED;
+  return cuda_status(p.kv_dtype == MLA_KV_BF16 ? launch_decode_tc(p, max_seq_len, stream)
+                                               : launch_decode_tc_fp8(p, stream));
 }
 
 mla_status mla_combine(const float* o_part, const float* lse_part, int B, int num_splits, int n_h,
