@@ -134,8 +134,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
   const uint32_t peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x >> 1;
-  const int b = unit / p.S, s = unit % p.S;
-  const int L = max(p.seq_lens[b], 0);
+  int L;
+  const int b = lpt_sequence(p, unit, reinterpret_cast<int*>(smem), &L), s = unit % p.S;
   int st, en;
   split_range(L, p.S, s, &st, &en);
   const int n_tiles = (en - st + kTile - 1) / kTile;
@@ -224,6 +224,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         const bool paged = p.block_table != nullptr;
         int issued = 0;
         HalfInfo h0{}, h1{};
+        int pg0 = page_ahead(p, b, st, 0), pg1 = page_ahead(p, b, st, 1);   // one tile ahead
         for (int k = 0; k < 3 * n_tiles; ++k) {
           const int i = k / 3, g = k % 3;
           const int r = group_slot(k), prior = group_prior_uses(k);
@@ -235,8 +236,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             break;
           }
           if (g == 0) {
-            h0 = half_info(p, b, st, en, 2 * i, true);
-            h1 = half_info(p, b, st, en, 2 * i + 1, true);
+            h0 = half_info(p, b, st, en, 2 * i, true, pg0);
+            h1 = half_info(p, b, st, en, 2 * i + 1, true, pg1);
+            pg0 = page_ahead(p, b, st, 2 * i + 2);
+            pg1 = page_ahead(p, b, st, 2 * i + 3);
           }
           unsigned char* dst = smem + S_RING + r * kGroup;
           const uint64_t pol = g < 2 ? pol_last : pol_first;   // chunk 8 (the RoPE key) is read once
@@ -341,6 +344,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       const uint32_t pfull_remote = mapa(smem_u32(&bars[VB_PFULL + j]), 1);
       // Every thread runs every iteration and every named barrier; after an abort the
       // waits return at once and the tiles are processed as fully masked.
+      int pg = page_ahead(p, b, st, j);   // this thread's half of the next tile, fetched ahead
       for (int i = 0; i < n_tiles; ++i) {
         uint32_t sr[64];
         const bool got = warp_wait(&bars[SB_SFULL], i & 1, abort_flag);
@@ -352,7 +356,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         }
         tc_fence_before();
         mbar_arrive(&bars[SB_SFREE]);
-        const int nv = got ? half_info(p, b, st, en, 2 * i + j, false).nvalid : 0;
+        const int nv = got ? half_info(p, b, st, en, 2 * i + j, false, pg).nvalid : 0;
+        pg = page_ahead(p, b, st, 2 * i + 2 + j);
         // Row maximum on the raw scores (the scale is positive); tokens past the split
         // (ragged tiles only) become -inf so that their weight is exactly 0.
         if (nv < 64) {
@@ -453,6 +458,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         int issued = 0;
         // Start once the score CTA has Q: its query load goes first.
         if (!mbar_wait<true>(&bars[VB_GO], 0, abort_flag, kWaitNs)) give_up(p, abort_flag, smem, peer);
+        int pg = page_ahead(p, b, st, 0);
         for (int u = 0; u < n_halves && !*abort_flag; ++u) {
           const int sg = u % kCStages;
           if (u >= kCStages &&
@@ -460,7 +466,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             give_up(p, abort_flag, smem, peer);
             break;
           }
-          const HalfInfo hi = half_info(p, b, st, en, u, false);
+          const HalfInfo hi = half_info(p, b, st, en, u, false, pg);
+          pg = page_ahead(p, b, st, u + 1);
           if (hi.load) {
             mbar_arrive_expect_tx(&bars[VB_CFULL + sg], kCStage);
             tma_load_3d(smem + V_CST + sg * kCStage, &vmap, &bars[VB_CFULL + sg], 0, hi.row0, 0, pol);
@@ -480,6 +487,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         int ncmd = 0, nflush = 0;
         bool ok = true, o_init = false;
         const volatile int never = 0;
+        int pg = page_ahead(p, b, st, 0);
         for (int u = 0; u < n_halves; ++u) {
           const int i = u >> 1, j = u & 1, sg = u % kCStages;
           if (!mbar_wait(&bars[VB_CFULL + sg], (u / kCStages) & 1, abort_flag, kWaitNs) ||
@@ -488,7 +496,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             break;
           }
           if (i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[VB_PFULL + j], j == 0 ? kPanel + kHdr : kPanel);
-          const HalfInfo hi = half_info(p, b, st, en, u, false);
+          const HalfInfo hi = half_info(p, b, st, en, u, false, pg);
+          pg = page_ahead(p, b, st, u + 1);
           const unsigned char* msg = smem + V_PANEL + j * kPanel;
           int c = 0;
           if (j == 0 && o_init && *reinterpret_cast<const volatile uint32_t*>(smem + V_HDR + 512) != 0u)

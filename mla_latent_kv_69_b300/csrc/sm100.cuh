@@ -161,6 +161,19 @@ __device__ __forceinline__ float ld_global_nc_or_zero(const float* ptr, bool pre
   return v;
 }
 
+// The same for a 32-bit integer, `dflt` when `pred` is false.
+__device__ __forceinline__ int ld_global_nc_or(const int* ptr, bool pred, int dflt) {
+  int v;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %2, 0;\n\t"
+      "mov.b32 %0, %3;\n\t"
+      "@q ld.global.nc.b32 %0, [%1];\n\t}"
+      : "=r"(v)
+      : "l"(ptr), "r"((int)pred), "r"(dflt));
+  return v;
+}
+
 // ------------------------------------ TMA -------------------------------------------
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
