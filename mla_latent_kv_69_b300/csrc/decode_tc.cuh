@@ -15,37 +15,6 @@ struct HalfInfo {
   bool load;    // some token is valid and its rows lie inside the caller's buffers
 };
 
-// For a paged cache (the variable-length layout) and batches up to kLptMaxB, clusters are
-// handed out longest sequence first: cluster r serves split r % S of the sequence whose
-// rank in the order (length descending, index ascending) is r / S. The splits of one
-// sequence are equal, so the longest units start first and the last wave holds the
-// shortest ones. Contiguous caches and larger batches keep the index order (the ranking
-// costs every unit ~1.5 us of start-up, measured, which uniform lengths do not repay).
-// Returns the sequence and stores its
-// length (clamped at 0) in *len. `scratch` is kLptMaxB + 1 ints of shared memory that
-// nothing writes until the caller's next CTA barrier; every thread of the CTA calls
-// this (it synchronises the CTA twice).
-constexpr int kLptMaxB = 256;
-__device__ __forceinline__ int lpt_sequence(const DecodeParams& p, int r, int* scratch, int* len) {
-  const int seq_rank = r / p.S;
-  if (p.B > kLptMaxB || !p.block_table) {
-    *len = max(p.seq_lens[seq_rank], 0);
-    return seq_rank;
-  }
-  for (int c = threadIdx.x; c < p.B; c += blockDim.x) scratch[c] = max(p.seq_lens[c], 0);
-  __syncthreads();
-  for (int c = threadIdx.x; c < p.B; c += blockDim.x) {
-    const int lc = scratch[c];
-    int rk = 0;
-    for (int o = 0; o < p.B; ++o) rk += (scratch[o] > lc || (scratch[o] == lc && o < c)) ? 1 : 0;
-    if (rk == seq_rank) scratch[kLptMaxB] = c;
-  }
-  __syncthreads();
-  const int b = scratch[kLptMaxB];
-  *len = scratch[b];
-  return b;
-}
-
 // Block-table entry of half u of the split that starts at token st (-1 past the table;
 // unused for contiguous caches). The predicated load writes its register by itself, so
 // a role can fetch the next half's entry while it works on this one and only stall, if

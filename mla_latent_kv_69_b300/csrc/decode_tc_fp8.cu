@@ -156,8 +156,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
   const uint32_t peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x >> 1;
-  int L;
-  const int b = lpt_sequence(p, unit, reinterpret_cast<int*>(smem), &L), s = unit % p.S;
+  const int b = unit / p.S, s = unit % p.S;
+  const int L = max(p.seq_lens[b], 0);
   int st, en;
   split_range(L, p.S, s, &st, &en);
   const int n_tiles = (en - st + kTile - 1) / kTile;
