@@ -3,7 +3,9 @@
 The functions mirror the C ABI in include/mla.h one to one. They only marshal
 arguments (shape/dtype/device checks, raw pointers, the current CUDA stream);
 every step of the computation runs in the library's CUDA kernels. Buffers are
-torch tensors on the GPU; outputs are allocated here when not passed in.
+torch tensors on the GPU; outputs are allocated here when not passed in. All tensors of
+a call must live on the current CUDA device (the library launches there, on the given
+stream or torch's current one).
 
 A decode step of one MLA layer:
 
@@ -66,6 +68,12 @@ def _need(t, name, dtype, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _need_table_rows(cache, B):
+    bt = cache.block_table
+    if bt is not None and (bt.dim() != 2 or bt.shape[0] < B):
+        raise ValueError(f"block_table must have a row per sequence: [>= {B}, max_pages]")
+
+
 @dataclass
 class Cache:
     """One layer's latent cache (see mla_cache in include/mla.h).
@@ -92,11 +100,15 @@ class Cache:
         c.dtype = self.dtype_code
         c.data = d.data_ptr()
         c.scales = _ptr(self.scales)
+        c.num_rows = d.shape[0] * d.shape[1]
         if self.scales is not None:
             _need(self.scales, "scales", torch.float32)
-        c.num_rows = d.shape[0] * d.shape[1]
+            if self.scales.numel() != c.num_rows:   # the kernels read one scale per row
+                raise ValueError(f"scales must hold one fp32 per cache row ({c.num_rows}), got {self.scales.numel()}")
         if self.block_table is not None:
             _need(self.block_table, "block_table", torch.int32)
+            if self.block_table.dim() != 2:
+                raise ValueError("block_table must be [B, max_pages]")
             if d.shape[1] != PAGE:
                 raise ValueError("paged cache data must be [pages, 64, 576]")
             c.block_table = self.block_table.data_ptr()
@@ -156,6 +168,7 @@ def decode_fwd(q_lat, cache: Cache, seq_lens, max_seq_len: int, softmax_scale: f
     _need(lse_part, "lse_part", torch.float32, (B, S, n_h))
     if status is not None:
         _need(status, "status", torch.int32)
+    _need_table_rows(cache, B)
     c = cache.to_c()
     scale = default_scale() if softmax_scale is None else float(softmax_scale)
     check("mla_decode_fwd", _lib.get().mla_decode_fwd(
@@ -191,6 +204,7 @@ def decode_combine_static(q_lat, cache: Cache, seq_lens, max_seq_len: int, o_lat
         _need(lse, "lse", torch.float32, (B, n_h))
     if status is not None:
         _need(status, "status", torch.int32)
+    _need_table_rows(cache, B)
     c = cache.to_c()
     scale = default_scale() if softmax_scale is None else float(softmax_scale)
     check("mla_decode_combine_static", _lib.get().mla_decode_combine_static(

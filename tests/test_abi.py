@@ -135,3 +135,17 @@ def test_static_entry_rejects_oversize_before_any_launch():
     assert rc == _lib.MLA_ERR_WORKSPACE
     assert _lib.get().mla_decode_combine_static(None, ctypes.byref(c), A, 32, 128, 4096, 0.07, 2, A, A, None,
                                                 None) == INVALID
+
+
+def test_binding_rejects_a_block_table_without_a_row_per_sequence():
+    import torch
+
+    import mla_latent_kv_69_b300 as mla
+
+    data = torch.zeros(4, 64, 576, dtype=torch.bfloat16)
+    ok = mla.Cache(data, None, torch.zeros(3, 2, dtype=torch.int32))
+    mla._need_table_rows(ok, 3)
+    with pytest.raises(ValueError):
+        mla._need_table_rows(ok, 4)
+    with pytest.raises(ValueError):
+        mla._need_table_rows(mla.Cache(data, None, torch.zeros(6, dtype=torch.int32)), 3)
