@@ -30,7 +30,7 @@ __all__ = [
     "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range", "decode_kernel",
     "decode_combine_static",
     "compute_dtype",
-    "Cache", "MlaError", "status_string", "default_scale", "decode_step", "lib_path",
+    "Cache", "MlaError", "status_string", "default_scale", "decode_step", "lib_path", "MLA_MAX_SPLITS",
 ]
 
 D_NOPE, D_ROPE, D_LATENT, D_ROW, D_Q, PAGE = 128, 64, 512, 576, 192, 64
