@@ -187,8 +187,9 @@ MLA_API mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t*
  *   launch. The array (MLA_STATIC_SCRATCH_BYTES on every GPU that loads the library,
  *   held until exit) is shared by all calls and keeps the last call's partials: calls
  *   that overlap on the GPU race, and the caller must serialise them. The first call
- *   on a device looks the array's device address up (cudaGetSymbolAddress) and should
- *   come before any stream capture. Allocates nothing.
+ *   on a device (and the first after a device reset replaced its context) looks the
+ *   array's device address up (cudaGetSymbolAddress) and should come before any stream
+ *   capture. Allocates nothing.
  */
 #define MLA_STATIC_SCRATCH_BYTES (32 << 20)
 MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens,

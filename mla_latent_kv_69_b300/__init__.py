@@ -4,8 +4,8 @@ The functions mirror the C ABI in include/mla.h one to one. They only marshal
 arguments (shape/dtype/device checks, raw pointers, the current CUDA stream);
 every step of the computation runs in the library's CUDA kernels. Buffers are
 torch tensors on the GPU; outputs are allocated here when not passed in. All tensors of
-a call must live on the current CUDA device (the library launches there, on the given
-stream or torch's current one).
+a call must live on one CUDA device (ValueError otherwise); the call runs with that
+device current, on the given stream or that device's current torch stream.
 
 A decode step of one MLA layer:
 
@@ -45,10 +45,35 @@ def default_scale() -> float:
     return 1.0 / math.sqrt(D_NOPE + D_ROPE)
 
 
-def _stream(stream) -> int:
+def _stream(stream, device=None) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _one_device(**tensors):
+    """The single CUDA device every given tensor lives on (None entries are skipped).
+
+    The library launches on the current device and dereferences every pointer there,
+    so a tensor on another GPU would hand a kernel a peer address."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        d = t.device
+        if dev is None:
+            dev = d
+        elif d != dev:
+            raise ValueError(f"{name} is on {d}, but the call's other tensors are on {dev}; "
+                             "every tensor of a call must be on one device")
+    return dev
+
+
+def _call(fn: str, device, *args, stream=None):
+    """Run one C-ABI call with `device` current, on `stream` (default: that device's
+    current torch stream), and raise MlaError on a non-OK status."""
+    with torch.cuda.device(device):
+        check(fn, getattr(_lib.get(), fn)(*args, _stream(stream, device)))
 
 
 def _ptr(t) -> int | None:
@@ -85,6 +110,10 @@ class Cache:
     data: torch.Tensor
     scales: torch.Tensor | None = None
     block_table: torch.Tensor | None = None
+
+    def tensors(self) -> dict:
+        """The cache's tensors by name (None where absent), for device checks."""
+        return {"cache.data": self.data, "cache.scales": self.scales, "cache.block_table": self.block_table}
 
     @property
     def dtype_code(self) -> int:
@@ -149,8 +178,8 @@ def absorb_q(q, w_uk, pos, q_lat=None, rope_base: float = 10000.0, stream=None):
     if q_lat is None:
         q_lat = torch.empty(B, n_h, D_ROW, dtype=torch.bfloat16, device=q.device)
     _need(q_lat, "q_lat", torch.bfloat16, (B, n_h, D_ROW))
-    check("mla_absorb_q", _lib.get().mla_absorb_q(_ptr(q), _ptr(w_uk), _ptr(pos), B, n_h, float(rope_base),
-                                                _ptr(q_lat), _stream(stream)))
+    dev = _one_device(q=q, w_uk=w_uk, pos=pos, q_lat=q_lat)
+    _call("mla_absorb_q", dev, _ptr(q), _ptr(w_uk), _ptr(pos), B, n_h, float(rope_base), _ptr(q_lat), stream=stream)
     return q_lat
 
 
@@ -170,10 +199,11 @@ def decode_fwd(q_lat, cache: Cache, seq_lens, max_seq_len: int, softmax_scale: f
         _need(status, "status", torch.int32)
     _need_table_rows(cache, B)
     c = cache.to_c()
+    dev = _one_device(q_lat=q_lat, seq_lens=seq_lens, o_part=o_part, lse_part=lse_part, status=status,
+                      **cache.tensors())
     scale = default_scale() if softmax_scale is None else float(softmax_scale)
-    check("mla_decode_fwd", _lib.get().mla_decode_fwd(
-        _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale, S,
-        _ptr(o_part), _ptr(lse_part), _ptr(status), _stream(stream)))
+    _call("mla_decode_fwd", dev, _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale, S,
+          _ptr(o_part), _ptr(lse_part), _ptr(status), stream=stream)
     return o_part, lse_part
 
 
@@ -187,8 +217,8 @@ def combine(o_part, lse_part, o_lat=None, lse=None, stream=None):
         lse = torch.empty(B, n_h, dtype=torch.float32, device=o_part.device)
     _need(o_lat, "o_lat", torch.float32, (B, n_h, D_LATENT))
     _need(lse, "lse", torch.float32, (B, n_h))
-    check("mla_combine", _lib.get().mla_combine(_ptr(o_part), _ptr(lse_part), B, S, n_h, _ptr(o_lat), _ptr(lse),
-                                              _stream(stream)))
+    dev = _one_device(o_part=o_part, lse_part=lse_part, o_lat=o_lat, lse=lse)
+    _call("mla_combine", dev, _ptr(o_part), _ptr(lse_part), B, S, n_h, _ptr(o_lat), _ptr(lse), stream=stream)
     return o_lat, lse
 
 
@@ -206,10 +236,10 @@ def decode_combine_static(q_lat, cache: Cache, seq_lens, max_seq_len: int, o_lat
         _need(status, "status", torch.int32)
     _need_table_rows(cache, B)
     c = cache.to_c()
+    dev = _one_device(q_lat=q_lat, seq_lens=seq_lens, o_lat=o_lat, lse=lse, status=status, **cache.tensors())
     scale = default_scale() if softmax_scale is None else float(softmax_scale)
-    check("mla_decode_combine_static", _lib.get().mla_decode_combine_static(
-        _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale, int(n_splits),
-        _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
+    _call("mla_decode_combine_static", dev, _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h,
+          int(max_seq_len), scale, int(n_splits), _ptr(o_lat), _ptr(lse), _ptr(status), stream=stream)
     return o_lat, lse
 
 
@@ -220,7 +250,8 @@ def up_v(o_lat, w_uv, o=None, stream=None):
     if o is None:
         o = torch.empty(B, n_h, D_NOPE, dtype=torch.float32, device=o_lat.device)
     _need(o, "o", torch.float32, (B, n_h, D_NOPE))
-    check("mla_up_v", _lib.get().mla_up_v(_ptr(o_lat), _ptr(w_uv), B, n_h, _ptr(o), _stream(stream)))
+    dev = _one_device(o_lat=o_lat, w_uv=w_uv, o=o)
+    _call("mla_up_v", dev, _ptr(o_lat), _ptr(w_uv), B, n_h, _ptr(o), stream=stream)
     return o
 
 
@@ -237,7 +268,8 @@ def quantize_fp8(rows, codes=None, scales=None, stream=None):
     _need(rows, "rows", torch.bfloat16)
     _need(codes, "codes", torch.uint8, (*lead, D_ROW))
     _need(scales, "scales", torch.float32, lead)
-    check("mla_quantize_fp8", _lib.get().mla_quantize_fp8(_ptr(rows), n, _ptr(codes), _ptr(scales), _stream(stream)))
+    dev = _one_device(rows=rows, codes=codes, scales=scales)
+    _call("mla_quantize_fp8", dev, _ptr(rows), n, _ptr(codes), _ptr(scales), stream=stream)
     return codes, scales
 
 

@@ -11,11 +11,13 @@
 // per GPU, which every GPU that loads the library holds until the process exits.
 //
 // On the host the array's name is only a stand-in symbol, not a device address, so
-// the address is looked up with cudaGetSymbolAddress once per device, with that
-// device current, by the first call made on it; that first call should come before
-// any stream capture. Every call uses the same array and leaves its partials there,
+// the address is looked up with cudaGetSymbolAddress once per device (and again after a
+// device reset has replaced the device's context), with that device current, by the
+// first call made there; that first call should come before any stream capture. Every call uses the same array and leaves its partials there,
 // so calls that overlap on the GPU (concurrent streams, or several host threads)
 // race and must be serialised by the caller.
+#include <cudaTypedefs.h>
+
 #include <climits>
 #include <mutex>
 
@@ -28,23 +30,53 @@ static __device__ __align__(256) unsigned char g_static_scratch[MLA_STATIC_SCRAT
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_static_scratch on the current device (nullptr on failure).
+// Unique id of the calling thread's current context (0 when it cannot be read). A
+// device reset destroys the primary context; the next one reloads the module, and the
+// array may then sit at another address, so the cached address is keyed on this id.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_static_scratch on the current device (nullptr on failure). It is
+// looked up once per device and context; without a readable context id it is looked up
+// on every call.
 void* scratch_address() {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {nullptr};
+  static unsigned long long ctx_of[kMaxDevices] = {0};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return nullptr;
   }
+  const unsigned long long ctx = current_context_id();   // 0 before the context exists
   std::lock_guard<std::mutex> g(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {   // makes the context current
       cudaGetLastError();
       return nullptr;
     }
     addr[dev] = p;
+    ctx_of[dev] = current_context_id();
   }
   return addr[dev];
 }

@@ -149,3 +149,20 @@ def test_binding_rejects_a_block_table_without_a_row_per_sequence():
         mla._need_table_rows(ok, 4)
     with pytest.raises(ValueError):
         mla._need_table_rows(mla.Cache(data, None, torch.zeros(6, dtype=torch.int32)), 3)
+
+
+def test_tensors_on_two_devices_are_rejected():
+    """Every tensor of a call must sit on one device: the library launches on the current
+    device and would otherwise be handed a peer GPU's address."""
+    from types import SimpleNamespace
+
+    import torch
+
+    d0 = SimpleNamespace(device=torch.device("cuda", 0))
+    d1 = SimpleNamespace(device=torch.device("cuda", 1))
+    assert mla._one_device(q_lat=d0, status=None, o_part=d0) == torch.device("cuda", 0)
+    assert mla._one_device(x=d1) == torch.device("cuda", 1)
+    with pytest.raises(ValueError, match="o_part"):
+        mla._one_device(q_lat=d0, o_part=d1)
+    with pytest.raises(ValueError, match="cache.block_table"):
+        mla._one_device(q_lat=d1, **{"cache.data": d1, "cache.block_table": d0})
