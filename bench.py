@@ -2,20 +2,27 @@
 """Benchmark of one MLA decode step (absorb_q → decode_fwd → combine → up_v) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload all|NAME] [--no-cpu-baseline]
 
 Prints ONE JSON line on rank 0. A "step" is one pass of the whole hot path over one
 batch of synthetic inputs; the latent cache and the weights are resident in HBM
 (they are the layer's state) and L2 is flushed (256 MiB write) before every timed
 step (the write is followed by a 256 MiB read so that no dirty lines of the flush
-are written back inside the timed kernels). `value` = latent-cache bytes per step ÷ step time (GB/s), summed over
-ranks; each rank decodes its own batch (weak scaling, no data-path collective).
-`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+are written back inside the timed kernels). `value` = latent-cache bytes per step ÷
+step time (GB/s), summed over ranks; each rank decodes its own batch (weak scaling,
+no data-path collective).
+
+The headline is the DeepSeek-V2 shape (B = 32 × 4096 tokens); with `--workload all`
+(the default) the other four workloads are measured in the same run and reported
+under "workloads", each with its own roofline, per-call times, e2e and CPU baseline.
+`--impl reference` times the fp64 CPU oracle on a fixed bounded sample instead.
 """
 from __future__ import annotations
 
 import argparse
+import gc
 import json
+import math
 import os
 import subprocess
 import sys
@@ -31,9 +38,20 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 METRIC = "MLA decode latent-cache GB/s, tokens/s, % HBM roofline on 1 B300"
-DEFAULT_WORKLOAD = "v2_b32_l4096"
+HEADLINE = "v2_b32_l4096"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# The oracle's bounded sample of each workload: (sequence, heads or None = all). The
+# same sample serves the CPU baseline of our arm and every step of the reference arm,
+# sized to a few seconds of fp64 work on a many-core host.
+ORACLE_SAMPLE = {
+    "tiny_h16_b1_l256": [(0, None)],
+    "v2_b32_l4096": [(b, None) for b in range(4)],
+    "paged_b64_l1k_32k": [(b, list(range(32))) for b in range(4)],
+    "long_b4_l128k": [(0, list(range(16)))],
+    "fp8_b128_l8192": [(b, list(range(64))) for b in range(8)],
+}
 
 
 # ------------------------------- distributed --------------------------------------
@@ -149,50 +167,98 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_oracle_sample(w: W.Workload, budget_s: float = 12.0, min_seqs: int = 1):
-    """Time the fp64 oracle (as it stands) on whole sequences of the workload until
-    the time budget is spent. Returns (GB/s of cache processed, seconds, sample text)."""
-    from oracle import fp8_e4m3, mla_oracle
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
 
-    lens = W.seq_lens(w)
-    qb, wk, wv = W.gen_q(w), W.bf16_bits_to_f32(W.gen_w_uk(w)), W.bf16_bits_to_f32(W.gen_w_uv(w))
-    order = list(np.argsort(lens, kind="stable"))          # cheapest sequences first keeps the bound
-    spent, done_bytes, seqs = 0.0, 0, []
-    per_tok = W.D_ROW * 2 if w.kv == "bf16" else W.D_ROW + 4
-    for b in order:
-        if spent >= budget_s and len(seqs) >= min_seqs:
-            break
-        L = int(lens[b])
-        rows = W.bf16_bits_to_f32(W.gen_rows(w, int(b), L))
-        if w.kv == "fp8":
-            codes, scales = fp8_e4m3.quantize_rows(rows)
-            rows = fp8_e4m3.dequantize_rows(codes, scales)
-        q = W.bf16_bits_to_f32(qb[b])
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return host_cores()
+
+
+def num_splits_for(w: W.Workload, lens) -> int:
+    """The split count the library resolves num_splits = 0 to (a host-only query)."""
+    import mla_latent_kv_69_b300 as mla
+
+    return mla.num_splits(w.batch, int(np.max(lens)) if len(lens) else 0, w.n_h)
+
+
+def workload_config(w: W.Workload, lens, n_splits: int) -> dict:
+    """`config` of a JSON line; both arms print the same dict for the same workload."""
+    return {"workload": w.name, "n_h": w.n_h, "batch_per_gpu": w.batch, "ctx": int(np.max(lens)),
+            "tokens_per_gpu": int(np.sum(lens, dtype=np.int64)), "kv": w.kv,
+            "layout": "paged-64" if w.paged else "contiguous", "n_splits": int(n_splits),
+            "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read; both outside the timed "
+                  "intervals); the cache of every workload but the tiny one is also larger than L2"}
+
+
+def oracle_sample_desc(w: W.Workload) -> str:
+    parts = [f"seq {b} ({'all' if h is None else len(h)} heads)" for b, h in ORACLE_SAMPLE[w.name]]
+    return f"{w.name}: " + ", ".join(parts) + "; fp64 explicit (non-absorbed) form"
+
+
+class OracleSample:
+    """The workload's fixed oracle sample, generated once; run() times one pass."""
+
+    def __init__(self, w: W.Workload):
+        from oracle import fp8_e4m3
+
+        self.w = w
+        lens = W.seq_lens(w)
+        qb = W.gen_q(w)
+        self.wk, self.wv = W.bf16_bits_to_f32(W.gen_w_uk(w)), W.bf16_bits_to_f32(W.gen_w_uv(w))
+        per_tok = W.D_ROW * 2 if w.kv == "bf16" else W.D_ROW + 4
+        self.items, self.bytes = [], 0.0
+        for b, heads in ORACLE_SAMPLE[w.name]:
+            L = int(lens[b])
+            rows = W.bf16_bits_to_f32(W.gen_rows(w, b, L))
+            if w.kv == "fp8":
+                codes, scales = fp8_e4m3.quantize_rows(rows)
+                rows = fp8_e4m3.dequantize_rows(codes, scales)
+            self.items.append((W.bf16_bits_to_f32(qb[b]), rows, heads, max(L - 1, 0)))
+            self.bytes += L * per_tok * (w.n_h if heads is None else len(heads)) / w.n_h
+
+    def run(self) -> float:
+        from oracle import mla_oracle
+
         t0 = time.perf_counter()
-        mla_oracle.attend_explicit(q, rows[:, :512], rows[:, 512:], wk, wv, pos_q=max(L - 1, 0))
-        spent += time.perf_counter() - t0
-        done_bytes += L * per_tok
-        seqs.append(int(b))
-    gbs = done_bytes / spent / 1e9 if spent > 0 else 0.0
-    return gbs, spent, f"{len(seqs)} whole sequence(s) {seqs[:4]}{'...' if len(seqs) > 4 else ''} of {w.name}, all {w.n_h} heads, fp64 explicit form"
+        for q, rows, heads, pos in self.items:
+            mla_oracle.attend_explicit(q, rows[:, :512], rows[:, 512:], self.wk, self.wv, pos_q=pos, heads=heads)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(w: W.Workload, budget_s: float) -> dict:
+    """The oracle as it stands, on the host cores, repeating the fixed sample for about
+    `budget_s` seconds: cache GB/s equivalent (bytes scaled by the heads evaluated)."""
+    smp = OracleSample(w)
+    spent, reps = 0.0, 0
+    while reps == 0 or spent < budget_s:
+        spent += smp.run()
+        reps += 1
+    return {"value": round(smp.bytes * reps / spent / 1e9, 5), "unit": "GB/s", "cores": _blas_threads(),
+            "kind": "oracle", "sample": oracle_sample_desc(w) + f"; {reps} pass(es)", "seconds": round(spent, 2)}
 
 
 # ------------------------------- our arm -------------------------------------------
-def run_ours(args, dist: Dist) -> dict | None:
+def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
+    """One workload on this rank's GPU: device-timed step (CUDA graph), per-call
+    intervals, end-to-end through the public call with host buffers, roofline."""
     import torch
 
     import mla_latent_kv_69_b300 as mla
 
-    torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
-    w = rank_workload(W.WORKLOADS[args.workload], dist.rank)
+    w = rank_workload(W.WORKLOADS[name], dist.rank)
     case = W.DeviceInputs(w, dev)
     if w.kv == "fp8":                     # the library's own cache writer makes the e4m3 cache
         codes, scales = mla.quantize_fp8(case.source)
-        case.cache = mla.Cache(codes, scales, case.block_table)
+        cache = mla.Cache(codes, scales, case.block_table)
         del case.source
     else:
-        case.cache = mla.Cache(case.source, None, case.block_table)
+        cache = mla.Cache(case.source, None, case.block_table)
     B, n_h = case.B, case.n_h
     S = mla.num_splits(B, case.max_len, n_h)
     bufs = dict(
@@ -213,17 +279,26 @@ def run_ours(args, dist: Dist) -> dict | None:
         # with a cold L2 that holds no dirty lines of the flush.
         flush.zero_()
         torch.sum(drain, dim=0, keepdim=True, out=drain_out)
+
     cache_bytes = W.cache_bytes(w, case.lens)
     weight_bytes = 2 * n_h * 128 * 512 * 2
     io_bytes = B * n_h * (192 * 2 + 576 * 2 * 2 + 128 * 4)     # q read, q_lat write+read, o write
     stream = torch.cuda.current_stream()
 
+    def call(i):
+        if i == 0:
+            mla.absorb_q(case.q, case.w_uk, case.pos, q_lat=bufs["q_lat"])
+        elif i == 1:
+            mla.decode_fwd(bufs["q_lat"], cache, case.seq_lens, case.max_len, n_splits=S,
+                           o_part=bufs["o_part"], lse_part=bufs["lse_part"])
+        elif i == 2:
+            mla.combine(bufs["o_part"], bufs["lse_part"], o_lat=bufs["o_lat"], lse=bufs["lse"])
+        else:
+            mla.up_v(bufs["o_lat"], case.w_uv, o=bufs["o"])
+
     def step():
-        mla.absorb_q(case.q, case.w_uk, case.pos, q_lat=bufs["q_lat"])
-        mla.decode_fwd(bufs["q_lat"], case.cache, case.seq_lens, case.max_len, n_splits=S,
-                       o_part=bufs["o_part"], lse_part=bufs["lse_part"])
-        mla.combine(bufs["o_part"], bufs["lse_part"], o_lat=bufs["o_lat"], lse=bufs["lse"])
-        mla.up_v(bufs["o_lat"], case.w_uv, o=bufs["o"])
+        for i in range(4):
+            call(i)
 
     for _ in range(args.warmup):
         step()
@@ -233,7 +308,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     # then the four library calls between two device-side events. Consecutive kernels of
     # the step overlap their launch and prologue with the previous kernel's tail
     # (programmatic dependent launch), so no event may sit between them in this graph;
-    # a second graph with events between the calls gives the per-kernel breakdown.
+    # a second graph with events between the calls gives the per-call breakdown.
     ev_step = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
     graph, graph_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
@@ -250,15 +325,9 @@ def run_ours(args, dist: Dist) -> dict | None:
         with torch.cuda.graph(graph_parts, stream=cap):
             flush_l2()
             ev[0].record()
-            mla.absorb_q(case.q, case.w_uk, case.pos, q_lat=bufs["q_lat"])
-            ev[1].record()
-            mla.decode_fwd(bufs["q_lat"], case.cache, case.seq_lens, case.max_len, n_splits=S,
-                           o_part=bufs["o_part"], lse_part=bufs["lse_part"])
-            ev[2].record()
-            mla.combine(bufs["o_part"], bufs["lse_part"], o_lat=bufs["o_lat"], lse=bufs["lse"])
-            ev[3].record()
-            mla.up_v(bufs["o_lat"], case.w_uv, o=bufs["o"])
-            ev[4].record()
+            for i in range(4):
+                call(i)
+                ev[i + 1].record()
     torch.cuda.current_stream().wait_stream(cap)
     for _ in range(max(args.warmup, 3)):
         graph.replay()
@@ -278,7 +347,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     dist.barrier()
     torch.cuda.synchronize()
     steps = []
-    for k in range(K):
+    for _ in range(K):
         graph.replay()
         torch.cuda.synchronize()
         steps.append(ev_step[0].elapsed_time(ev_step[1]))   # ms
@@ -286,7 +355,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     dist.barrier()
     clocks = sampler.stop()
     per = []
-    for k in range(K):
+    for _ in range(K):
         graph_parts.replay()
         torch.cuda.synchronize()
         per.append([ev[i].elapsed_time(ev[i + 1]) for i in range(4)])   # ms
@@ -296,34 +365,33 @@ def run_ours(args, dist: Dist) -> dict | None:
     step_ms_max = dist.max(step_ms, dev)
 
     # e2e through the public API with host buffers: per step, H2D of the new queries
-    # (+ positions, lengths) from pinned memory and D2H of the outputs o.
+    # (+ positions, lengths) from pinned memory, the four calls, and D2H of o.
     h_q = case.q.cpu().pin_memory()
     h_pos = case.pos.cpu().pin_memory()
     h_len = case.seq_lens.cpu().pin_memory()
     h_o = torch.empty(B, n_h, 128, dtype=torch.float32).pin_memory()
     d_q, d_pos, d_len = torch.empty_like(case.q), torch.empty_like(case.pos), torch.empty_like(case.seq_lens)
+    e2e_bufs = dict(bufs)
 
     def e2e_step():
         d_q.copy_(h_q, non_blocking=True)
         d_pos.copy_(h_pos, non_blocking=True)
         d_len.copy_(h_len, non_blocking=True)
-        mla.absorb_q(d_q, case.w_uk, d_pos, q_lat=bufs["q_lat"])
-        mla.decode_fwd(bufs["q_lat"], case.cache, d_len, case.max_len, n_splits=S,
-                       o_part=bufs["o_part"], lse_part=bufs["lse_part"])
-        mla.combine(bufs["o_part"], bufs["lse_part"], o_lat=bufs["o_lat"], lse=bufs["lse"])
-        mla.up_v(bufs["o_lat"], case.w_uv, o=bufs["o"])
-        h_o.copy_(bufs["o"], non_blocking=True)
+        mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=S, bufs=e2e_bufs)
+        h_o.copy_(e2e_bufs["o"], non_blocking=True)
 
     for _ in range(max(args.warmup, 1)):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
+    e2e_ms, host_ms = [], []
     for _ in range(K):
         flush_l2()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
+        t0 = time.perf_counter()
         e2e_step()
+        host_ms.append(1e3 * (time.perf_counter() - t0))
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
@@ -337,7 +405,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     achieved = cache_bytes / (decode_ms / 1e3) / 1e9
     # Which pipe bounds the decode kernel: QK^T over 576 and PV over 512 columns per
     # (token, head) against the cache bytes; a bf16 cache sits just under the measured
-    # ridge (HBM-bound), an e4m3 cache, whose f16 MMAs run on dequantised codes, above it.
+    # ridge (HBM-bound), an e4m3 cache, whose f16 MMAs run on converted codes, above it.
     flops = 2.0 * (576 + 512) * n_h * float(np.sum(case.lens))
     tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))   # f16 dense = bf16 dense
     tensor_bound = flops / cache_bytes > tensor_peak * 1e12 / (hbm_peak * 1e9)
@@ -347,70 +415,78 @@ def run_ours(args, dist: Dist) -> dict | None:
     if os.path.exists(prof):
         with open(prof) as f:
             pj = json.load(f)
-        if pj.get("workload") == w.name and pj.get("kernel_source_hash") == _kernel_hash():
-            traffic = pj.get("dram_bytes_per_launch")
-    if dist.rank != 0:
-        return None
+        rec = pj.get(w.name) if isinstance(pj, dict) else None
+        if rec and rec.get("kernel_source_hash") == _kernel_hash():
+            traffic = rec.get("dram_bytes_per_launch")
+    roof_common = {"kernel": "mla_decode_fwd", "traffic": traffic, "algorithmic_bytes_per_launch": cache_bytes,
+                   "algorithmic_flops_per_launch": flops}
+    if tensor_bound:
+        roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": tensor_peak,
+                    "unit": "TFLOP/s", "frac": round(achieved_tflops / tensor_peak, 4),
+                    "peak_source": f"{peaks_src} bf16_tflops (the f16 dense rate is the same)",
+                    "hbm_achieved_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4),
+                    **roof_common}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peaks_src} hbm_gbs",
+                    "tensor_achieved_tflops": round(achieved_tflops, 1),
+                    "tensor_frac": round(achieved_tflops / tensor_peak, 4), **roof_common}
     res = {
         "metric": METRIC,
         "value": round(value, 2),
         "unit": "GB/s",
-        "n_gpus": dist.world,
-        "steps": K,
-        "warmup": args.warmup,
         "ms_per_step": round(step_ms_max, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": _compute_dtype(w, n_h),
-        "data": "synthetic (seeded N(0,1) bf16 cache and queries, N(0,1/512) weights; no checkpoint)",
-        "config": {
-            "workload": w.name, "n_h": n_h, "batch_per_gpu": B, "ctx": int(case.max_len), "kv": w.kv,
-            "layout": "paged-64" if w.paged else "contiguous", "n_splits": S,
-            "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read that drains the written lines; both outside the timed intervals)",
-            "timing": "CUDA-graph replay of the step between two device-side events; kernel_ms from a second graph with events between the four calls",
-            "decode_kernel": mla.decode_kernel(w.kv, n_h),
-            "step": "absorb_q + decode_fwd + combine + up_v, one MLA layer",
-        },
+        "dtype": mla.compute_dtype(n_h, w.kv),
+        "config": workload_config(w, case.lens, S),
         "decode_tokens_per_s": round(B * dist.world / (step_ms_max / 1e3), 1),
-        "hbm_roofline_frac_step": round((cache_bytes + weight_bytes + io_bytes) / (step_ms / 1e3) / 1e9 / hbm_peak, 4),
+        "decode_tokens_per_s_note": "sequences decoded per second, one MLA layer",
+        "hbm_roofline_frac_step": round((cache_bytes + weight_bytes + io_bytes) / (step_ms / 1e3) / 1e9 / hbm_peak,
+                                        4),
         "kernel_ms": {"absorb_q": round(float(kern_ms[0]), 5), "decode_fwd": round(decode_ms, 5),
                       "combine": round(float(kern_ms[2]), 5), "up_v": round(float(kern_ms[3]), 5)},
-        "roofline": ({"kernel": "mla_decode_fwd", "bound": "tensor", "achieved": round(achieved_tflops, 1),
-                      "peak": tensor_peak, "unit": "TFLOP/s", "frac": round(achieved_tflops / tensor_peak, 4),
-                      "traffic": traffic, "peak_source": f"{peaks_src} bf16_tflops (the f16 dense rate is the same)",
-                      "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": cache_bytes,
-                      "hbm_achieved_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4)}
-                     if tensor_bound else
-                     {"kernel": "mla_decode_fwd", "bound": "hbm", "achieved": round(achieved, 1),
-                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                      "traffic": traffic, "peak_source": f"{peaks_src} hbm_gbs",
-                      "algorithmic_bytes_per_launch": cache_bytes, "algorithmic_flops_per_launch": flops,
-                      "tensor_achieved_tflops": round(achieved_tflops, 1),
-                      "tensor_frac": round(achieved_tflops / tensor_peak, 4)}),
+        "decode_kernel": mla.decode_kernel(w.kv, n_h),
+        "roofline": roofline,
         "cache_gbs_decode_combine": round(cache_bytes / ((decode_ms + float(kern_ms[2])) / 1e3) / 1e9, 1),
         "e2e": {"value": round(total_cache / (e2e_mean / 1e3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_mean, 5),
+                "ms_per_step": round(e2e_mean, 5), "host_ms_per_step": round(float(np.mean(host_ms)), 4),
                 "h2d_bytes_per_step": int(h_q.numel() * 2 + h_pos.numel() * 4 + h_len.numel() * 4),
-                "d2h_bytes_per_step": int(h_o.numel() * 4)},
-        "gpu_launches": 4 * K,
-        "kernel_ms_note": "per-call intervals from a graph with events between the calls (no launch overlap there); their sum exceeds ms_per_step",
+                "d2h_bytes_per_step": int(h_o.numel() * 4),
+                "path": "mla.decode_step (the public Python call over the C ABI) with pinned host buffers"},
         "clocks": {**clocks, "window": f"{args.soak:.1f} s soak + the timed steps"},
     }
-    if not args.no_cpu_baseline and dist.world == 1:
-        gbs, spent, sample = cpu_oracle_sample(w, budget_s=args.cpu_budget)
-        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": _blas_threads(),
-                               "kind": "oracle", "sample": sample, "seconds": round(spent, 2)}
+    del case, cache, bufs, e2e_bufs, flush, drain, graph, graph_parts
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline and dist.world == 1 and dist.rank == 0:
+        res["cpu_baseline"] = cpu_baseline(W.WORKLOADS[name], args.cpu_budget if headline else args.cpu_budget / 2)
     return res
 
 
-def _compute_dtype(w, n_h) -> str:
-    try:
-        import mla_latent_kv_69_b300 as mla
+def run_ours(args, dist: Dist) -> dict | None:
+    import torch
 
-        return mla.compute_dtype(n_h, w.kv)
-    except AttributeError:
-        return "f32"
+    torch.cuda.set_device(dist.local_rank)
+    names = [HEADLINE] + [n for n in W.WORKLOAD_ORDER if n != HEADLINE] if args.workload == "all" else [args.workload]
+    recs = {n: measure_ours(n, args, dist, headline=(i == 0)) for i, n in enumerate(names)}
+    if dist.rank != 0:
+        return None
+    head = recs[names[0]]
+    res = {
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": head["dtype"],
+        "data": "synthetic (seeded N(0,1) bf16 cache and queries, N(0,1/512) weights; no checkpoint)",
+        **{k: v for k, v in head.items() if k not in ("metric", "value", "unit", "ms_per_step", "dtype")},
+        "gpu_launches": 4 * args.steps,
+        "timing": "CUDA-graph replay of the step between two device-side events; kernel_ms from a second graph "
+                  "with events between the four calls (no launch overlap there, so they sum to more than the step)",
+        "step": "absorb_q + decode_fwd + combine + up_v, one MLA layer",
+    }
+    if len(names) > 1:
+        res["workloads"] = {n: recs[n] for n in names[1:]}
+        res["gpu_launches_all_workloads"] = 4 * args.steps * len(names)
+    return res
 
 
 def _kernel_hash() -> str:
@@ -424,44 +500,32 @@ def _kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def _blas_threads() -> int:
-    try:
-        from threadpoolctl import threadpool_info
-
-        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
-    except Exception:
-        pass
-    return host_cores()
-
-
 # ------------------------------- reference arm -------------------------------------
 def run_reference(args, dist: Dist) -> dict | None:
-    """The oracle as it stands, on the host cores, rank 0 only."""
+    """The oracle as it stands, on the host cores, rank 0 only: each step is one pass of
+    the headline workload's fixed oracle sample."""
     if dist.rank != 0:
         return None
-    w = W.WORKLOADS[args.workload]
-    per_step_budget = max(1.0, args.ref_budget / max(args.steps + args.warmup, 1))
+    name = HEADLINE if args.workload == "all" else args.workload
+    w = W.WORKLOADS[name]
+    lens = W.seq_lens(w)
+    smp = OracleSample(w)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, budget_s=per_step_budget)
-    vals, secs, sample = [], [], ""
-    for _ in range(args.steps):
-        gbs, spent, sample = cpu_oracle_sample(w, budget_s=per_step_budget)
-        vals.append(gbs)
-        secs.append(spent)
-    value = float(np.mean(vals))
+        smp.run()
+    secs = [smp.run() for _ in range(args.steps)]
+    mean_s = float(np.mean(secs))
+    value = smp.bytes / mean_s / 1e9
     return {
-        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(secs)), 2),
+        "metric": METRIC, "impl": "reference", "value": round(value, 5), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * mean_s, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 cache and queries, N(0,1/512) weights; no checkpoint)",
-        "config": {"workload": w.name, "n_h": w.n_h, "batch_per_gpu": w.batch, "kv": w.kv,
-                   "layout": "paged-64" if w.paged else "contiguous",
-                   "step": "fp64 oracle, explicit form, on a bounded sample of whole sequences"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": workload_config(w, lens, num_splits_for(w, lens)),
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": oracle_sample_desc(w), "seconds": round(float(np.sum(secs)), 2)},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "step": "one pass of the fp64 oracle (explicit form) over the fixed sample; GB/s counts the sample's "
+                "cache bytes scaled by the heads evaluated",
     }
 
 
@@ -471,12 +535,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
+    ap.add_argument("--workload", default="all", choices=["all"] + list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before the timed steps "
                     "(nvidia-smi clock samples span soak + timed region)")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--ref-budget", type=float, default=60.0, help="total oracle seconds for --impl reference")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="oracle seconds for the headline cpu_baseline "
+                    "(half of it for each other workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -8,19 +8,26 @@
 //
 // A kind::f16 MMA takes two operands of one type and an 8-bit query would not keep the
 // error budget, so both contractions run on f16 operands: every e4m3 code maps to the f16
-// of 2^-8 times its value, which is exact (see e4m3x16_to_f16), and the query converts
-// from bf16 to f16 exactly within f16's range (11 significant bits against bf16's 8).
-// The 2^8 comes back in fp32:
-// in the score scale and in the output's 1/l. Each CTA has four converter warps that
+// of 2^-8 times its value, which is exact (see e4m3x16_to_f16), and each head's query is
+// multiplied by a power of two 2^k_h that puts its largest element in [2^14, 2^15) before
+// it converts from bf16 to f16 (11 significant bits against bf16's 8), so no query
+// overflows f16 or loses its significant elements to f16's subnormal range.
+// The 2^8 and 2^-k_h come back in fp32, in the score scale and in the output's 1/l.
+// Each CTA has four converter warps that
 // turn TMA-loaded e4m3 rows into 128B-swizzled f16 operand tiles:
 //   score CTA  e4m3 ring of five 24 KB groups (128 tokens x 3 column chunks) →
 //              four 16 KB f16 slots (128 tokens x 64 columns) → 4 MMAs each;
 //   value CTA  e4m3 ring of two 32 KB steps (64 tokens x 512 columns) → two 64 KB f16
 //              stages → 8 MMAs of N = 256 per step (rows past the split are zeroed).
-// The per-token scale stays outside the MMAs: the score CTA multiplies each score column
-// by it (s_t = scale_t · Q·code_t) and each P column by it before P leaves for the value
-// CTA (O += (p_t · scale_t) · code_t, P in f16), while the softmax normaliser sums the
-// unscaled p. Every wait is bounded as in the bf16 kernel.
+// The per-token scale stays outside the MMAs. The score CTA multiplies each score column
+// by it (x_t = scale_t · Q·code_t, log2 units) and runs the online softmax on the log2
+// weight of the codes, y_t = x_t + log2 scale_t: the value CTA receives P'_t = 2^(y_t - m)
+// in f16 and accumulates O += P'_t · code_t, and the normaliser sums
+// 2^(x_t - m) = P'_t / scale_t in fp32. Since the running maximum m is taken over y, every
+// P' that matters lies in f16's normal range (at most 2^8 under the lazy maximum) however
+// small or large the tokens' scales are; folding scale_t into p instead would leave the
+// top weight at amax/448, subnormal in f16 for rows of small magnitude. Every wait is
+// bounded as in the bf16 kernel.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -62,8 +69,9 @@ constexpr int S_F16 = S_E4 + kE4Ring * kE4Group;
 constexpr int S_PANEL = S_F16 + kF16Ring * kF16Slot;
 constexpr int S_HDR = S_PANEL + 2 * kPanel;
 constexpr int S_MX = S_HDR + 1024;
-constexpr int S_SCL = S_MX + 1024;         // [2 tiles][128] fp32 per-token scales
-constexpr int S_END = S_SCL + 1024;
+constexpr int kSclBuf = 3 * 128;           // per tile: scale_t, log2 scale_t, 1 / scale_t (fp32)
+constexpr int S_SCL = S_MX + 1024;         // [2 tiles][kSclBuf] fp32
+constexpr int S_END = S_SCL + 2 * kSclBuf * 4;
 //   value CTA
 constexpr int V_E4 = 0;
 constexpr int V_F16 = V_E4 + 2 * kVE4;
@@ -147,7 +155,8 @@ __device__ __forceinline__ void convert_unit(const unsigned char* src, unsigned 
   *reinterpret_cast<uint4*>(dst_row + (((2 * c16 + 1) ^ (row & 7)) << 4)) = hi;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// 14 warps x 144 registers = 64,512 of the SM's 65,536 (the default cap of 128 spills)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(144)
 decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e4s_map,
                      const __grid_constant__ CUtensorMap e4v_map, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap omap, float scale_log2) {
@@ -332,7 +341,15 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
           ok = false;
           break;
         }
-        scl[(i & 1) * 128 + r] = sc_next;
+        {
+          // rows past the split (scale 0) get log2 = -inf and 1/scale = 0; their scores
+          // are masked to -inf anyway
+          float* sb = scl + (i & 1) * kSclBuf;
+          const bool pos = sc_next > 0.f;
+          sb[r] = sc_next;
+          sb[128 + r] = pos ? __log2f(sc_next) : -INFINITY;
+          sb[256 + r] = pos ? 1.f / sc_next : 0.f;
+        }
         mbar_arrive(&bars[SB_SCLREADY + (i & 1)]);
         sc_next = row_scale(i + 1);
         for (int c = 0; c < 9; ++c) {
@@ -370,9 +387,37 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       const int h = q * 32 + lane;
       const int j = (warp - 2) >> 2;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      // Q rows → TMEM as f16 pairs (rounded from bf16; heads beyond n_h are zero)
+      // Q rows → TMEM as f16 pairs. Each head's row is first multiplied by a power of two
+      // 2^k_h that brings its largest magnitude into [2^14, 2^15), so that the bf16 →
+      // f16 conversion neither overflows nor goes subnormal for the elements that
+      // matter; 2^-k_h comes back in fp32 with the scores (heads beyond n_h are zero).
       const int qrows = p.n_h < 128 ? p.n_h : 128;
-      if (warp_wait(&bars[SB_QFULL], 0, abort_flag)) {
+      const bool qok = warp_wait(&bars[SB_QFULL], 0, abort_flag);
+      uint32_t qmax = 0;   // largest |q| of this thread's chunks, as bf16 magnitude bits
+      if (qok && h < p.n_h) {
+#pragma unroll 1
+        for (int c = j; c < 9; c += 2) {
+          const unsigned char* row = smem + S_E4 + (c / 3) * kQGroup + (c % 3) * (qrows * 128) + h * 128;
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((x ^ (h & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+          }
+        }
+      }
+      uint32_t* qmx = reinterpret_cast<uint32_t*>(smem + S_MX);
+      qmx[j * 128 + h] = qmax;
+      named_sync(1, 256);
+      qmax = max(qmx[h], qmx[128 + h]);
+      // later writes of this region come after the first tile's vote (a barrier of the
+      // same 256 threads), so these reads cannot see them
+      const int qexp = (int)((qmax >> 7) & 0xFFu);   // biased bf16 exponent of max |q|
+      const int qk = qmax == 0u ? 0 : min(126, max(-126, 141 - qexp));
+      const float qmul = __uint_as_float((uint32_t)(127 + qk) << 23);   // 2^k_h
+      const float qsl = __uint_as_float((uint32_t)(127 - qk) << 23) * scale_log2;   // 2^-k_h · scale · log2 e · 2^8
+      if (qok) {
 #pragma unroll 1
         for (int c = j; c < 9; c += 2) {
           uint32_t rg[32];
@@ -385,7 +430,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-              const __half2 hv = __floats2half2_rn(f2.x, f2.y);
+              const __half2 hv = __floats2half2_rn(f2.x * qmul, f2.y * qmul);
               rg[4 * x + e] = *reinterpret_cast<const uint32_t*>(&hv);
             }
           }
@@ -417,16 +462,22 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         mbar_arrive(&bars[SB_SFREE]);
         const bool sok = warp_wait(&bars[SB_SCLREADY + (i & 1)], (i >> 1) & 1, abort_flag);
         const int nv = (got && sok) ? half_info(p, b, st, en, 2 * i + j, false).nvalid : 0;
-        const float4* sc4 = reinterpret_cast<const float4*>(scl + (i & 1) * 128 + 64 * j);
-        // x_t = s_t · scale_t · log2(e)/sqrt(d): the score of the dequantised token
+        const float* sb = scl + (i & 1) * kSclBuf;
+        const float4* sc4 = reinterpret_cast<const float4*>(sb + 64 * j);
+        const float4* ls4 = reinterpret_cast<const float4*>(sb + 128 + 64 * j);
+        // x_t = s_t · scale_t · 2^-k_h · log2(e)/sqrt(d) is the log2 score of the
+        // dequantised token; the softmax runs on y_t = x_t + log2 scale_t, the log2 of
+        // its weight on the codes, so that P' = 2^(y_t - m) stays within f16's normal
+        // range whatever the token's scale.
 #pragma unroll
         for (int t4 = 0; t4 < 16; ++t4) {
-          const float4 c4 = sc4[t4];
+          const float4 c4 = sc4[t4], l4 = ls4[t4];
           const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+          const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int t = 4 * t4 + e;
-            sr[t] = __float_as_uint(t < nv ? __uint_as_float(sr[t]) * (cc[e] * scale_log2) : -INFINITY);
+            sr[t] = __float_as_uint(t < nv ? fmaf(__uint_as_float(sr[t]), cc[e] * qsl, ll[e]) : -INFINITY);
           }
         }
         float m8[8];
@@ -453,7 +504,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
           }
         }
         const uint32_t nres = nneed ? named_popc(1, 256, row_rescale) : 0u;
-        // p = 2^(x - m); the normaliser sums p, the value CTA receives p · scale_t (f16).
+        // P' = 2^(y - m) goes to the value CTA (f16); the normaliser sums
+        // 2^(x - m) = P' / scale_t in fp32.
         // Each 8-token slice is packed and stored at once (the panel must be free first:
         // the value CTA's PV on the previous tile has read it), which keeps the thread
         // within the register budget of a 14-warp CTA.
@@ -470,14 +522,14 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int t = 8 * c8 + 2 * e;
-            const float2 sc2 = reinterpret_cast<const float2*>(scl + (i & 1) * 128 + 64 * j)[t >> 1];
+            const float2 is2 = reinterpret_cast<const float2*>(sb + 256 + 64 * j)[t >> 1];
             float2 pp = make_float2(0.f, 0.f);
             if (live) {
               const float2 xy = fadd2(make_float2(__uint_as_float(sr[t]), __uint_as_float(sr[t + 1])), nm2);
               pp = make_float2(ex2(xy.x), ex2(xy.y));
             }
-            acc = fadd2(acc, pp);
-            const __half2 v = __floats2half2_rn(pp.x * sc2.x, pp.y * sc2.y);
+            acc = ffma2(pp, is2, acc);
+            const __half2 v = __floats2half2_rn(pp.x, pp.y);
             pk[e] = *reinterpret_cast<const uint32_t*>(&v);
           }
           *reinterpret_cast<uint4*>(stg + h * 128 + ((c8 ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -540,7 +592,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        // ---- O += (p · scale) · code, 8 MMAs of 128 x 256 x 16 per 64-token step ----
+        // ---- O += P' · code, 8 MMAs of 128 x 256 x 16 per 64-token step ----
         const uint32_t idv = idesc_f16(128, 256, /*fp16_inputs=*/true, false, true);
         int ncmd = 0, nflush = 0;
         bool ok = true, o_init = false;

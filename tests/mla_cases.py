@@ -35,6 +35,39 @@ class Case(W.DeviceInputs):
         else:
             self.cache = mla.Cache(self.source, None, self.block_table)
 
+    def rebuild_cache(self):
+        """Re-make the library's cache view after `source` changed (re-quantises e4m3)."""
+        import mla_latent_kv_69_b300 as mla
+
+        if self.w.kv == "fp8":
+            codes, scales = mla.quantize_fp8(self.source)
+            self.cache = mla.Cache(codes, scales, self.block_table)
+        else:
+            self.cache = mla.Cache(self.source, None, self.block_table)
+
+    def set_rows(self, b: int, tokens, rows_bits: np.ndarray):
+        """Overwrite cache rows (bf16 bits [len(tokens), 576]) of sequence b on the host
+        copy and in the device `source`; call rebuild_cache() afterwards."""
+        import torch
+
+        tokens = np.asarray(tokens, dtype=np.int64)
+        host = self.rows_of(b).copy()
+        host[tokens] = rows_bits
+        self.rows[b] = host
+        dev_rows = bits_to_torch_bf16(np.ascontiguousarray(rows_bits), self.device)
+        if self.block_table_np is None:
+            self.source[b, torch.from_numpy(tokens).to(self.device)] = dev_rows
+        else:
+            pages = self.block_table_np[b, tokens // 64].astype(np.int64)
+            self.source[torch.from_numpy(pages).to(self.device), torch.from_numpy(tokens % 64).to(self.device)] = dev_rows
+
+    def scale_queries(self, factor):
+        """Multiply the queries by `factor` (a number, or one per sequence), rounded to
+        bf16, on the host and the device."""
+        f = np.broadcast_to(np.asarray(factor, np.float32), (self.B,))[:, None, None]
+        self.q_bits = W.f32_to_bf16_bits(rows_f32(self.q_bits) * f)
+        self.q = bits_to_torch_bf16(self.q_bits, self.device)
+
     def run(self, n_splits: int = 0, status=None, bufs=None):
         import mla_latent_kv_69_b300 as mla
 

@@ -32,7 +32,9 @@ def _compare(case, out, samples, check_lat=True):
         got.append(o[b, hs]); ref.append(r["o"][hs])
         got_lat.append(o_lat[b, hs]); ref_lat.append(r["o_lat"][hs])
         if case.lens[b] > 0:
-            np.testing.assert_allclose(lse[b, hs], r["lse"][hs], atol=2e-2, rtol=0)
+            # lse carries the score error of the bf16 query (2^-9 relative per element),
+            # which grows with the scores' magnitude; the fp32 normaliser adds ~1e-6
+            np.testing.assert_allclose(lse[b, hs], r["lse"][hs], atol=4e-3, rtol=2e-3)
         else:
             assert np.all(np.isneginf(lse[b, hs]))
     got, ref = np.concatenate([g.ravel() for g in got]), np.concatenate([r.ravel() for r in ref])
@@ -55,6 +57,9 @@ SMALL = [
     ("h32_paged", W.Workload("s6", n_h=32, batch=2, ctx=0, paged=True, seed=8), [300, 129]),
     ("h16", W.Workload("s7", n_h=16, batch=2, ctx=0, seed=9), [513, 2]),
     ("with_empty_seq", W.Workload("s8", n_h=128, batch=3, ctx=0, seed=10), [0, 191, 64]),
+    ("h64_fp8", W.Workload("s9", n_h=64, batch=2, ctx=0, kv="fp8", seed=11), [300, 129]),
+    ("h32_fp8_paged", W.Workload("s10", n_h=32, batch=2, ctx=0, kv="fp8", paged=True, seed=12), [513, 70]),
+    ("h16_fp8", W.Workload("s11", n_h=16, batch=2, ctx=0, kv="fp8", seed=13), [257, 2]),
 ]
 
 
@@ -141,7 +146,8 @@ FULL = {
     "v2_b32_l4096": lambda c: [(0, None), (c.B - 1, None)],
     "paged_b64_l1k_32k": lambda c: [(int(np.argmin(c.lens)), None), (int(np.argmax(c.lens)), [0, 1, 2, 127]),
                                     (0, list(range(0, 128, 16)))],
-    "long_b4_l128k": lambda c: [(0, [0, 77]), (3, [127])],
+    "long_b4_l128k": lambda c: [(0, list(range(0, 128, 16))), (1, [5, 64, 101]), (2, [30, 127]),
+                                (3, list(range(3, 128, 24)))],
     "fp8_b128_l8192": lambda c: [(0, list(range(0, 128, 4))), (127, list(range(1, 128, 8)))],
 }
 
@@ -162,3 +168,122 @@ def test_full_size_sampled(cuda_device, name):
     del case, out
     gc.collect()
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------------------------
+# The lazy running maximum: a head's maximum is raised only when a tile beats it by more
+# than 2^8 (log2 units), and then the value CTA rescales that head's rows of O in TMEM.
+# N(0, 1) inputs never trigger it after the first tile, so these cases plant tokens whose
+# latent lies along the heads' absorbed queries with growing strength.
+# ------------------------------------------------------------------------------------
+SPIKES = [(300, 300.0), (700, 600.0), (1600, 1100.0), (2990, 2000.0)]   # (token, strength)
+
+
+def _absorbed_direction(case, b):
+    """Unit vector along sum_h W_UK[h]^T q^C[b, h] (fp64, test-side)."""
+    q = rows_f32(case.q_bits[b]).astype(np.float64)
+    wk = rows_f32(case.wuk_bits).astype(np.float64)
+    g = np.einsum("hd,hdj->j", q[:, :128], wk)
+    return g / np.linalg.norm(g)
+
+
+def _plant_spikes(case, spikes):
+    for b in range(case.B):
+        g = _absorbed_direction(case, b)
+        toks = [t for t, _ in spikes if t < case.lens[b]]
+        rows = np.zeros((len(toks), 576), np.float32)
+        for k, (t, a) in enumerate(spikes[:len(toks)]):
+            rows[k, :512] = a * g
+        case.set_rows(b, toks, W.f32_to_bf16_bits(rows))
+    case.rebuild_cache()
+
+
+def _count_rescales(case, b, n_splits):
+    """Rescales of O the kernel's schedule performs for sequence b (heads x events),
+    replayed on the oracle's scores: per split, per 128-token tile, a head whose tile
+    maximum exceeds its running maximum by more than 8 (log2) after the first raise.
+    For an e4m3 cache the running maximum is taken over the score plus log2 of the
+    token's scale (the log2 weight of the codes)."""
+    rows = case.oracle_rows(b)
+    q = rows_f32(case.q_bits[b])
+    from oracle import mla_oracle
+    out = mla_oracle.attend_explicit(q, rows[:, :512], rows[:, 512:], rows_f32(case.wuk_bits),
+                                     rows_f32(case.wuv_bits), pos_q=int(case.pos_np[b]), return_p=True)
+    with np.errstate(divide="ignore"):
+        y = (np.log(out["p"]) + out["lse"][:, None]) / np.log(2.0)
+    if case.w.kv == "fp8":
+        _, scales = fp8_e4m3.quantize_rows(rows_f32(case.rows_of(b)))
+        y = y + np.log2(scales.astype(np.float64))[None, :]
+    L = int(case.lens[b])
+    events = 0
+    for sp in range(n_splits):
+        st, en = mla.split_range(L, n_splits, sp)
+        m = np.full(case.n_h, -np.inf)
+        for t0 in range(st, en, 128):
+            mt = y[:, t0:min(t0 + 128, en)].max(axis=1)
+            rise = mt > m + 8.0
+            events += int(np.sum(rise & np.isfinite(m)))
+            m = np.where(rise, mt, m)
+    return events
+
+
+RESCALE = [
+    ("bf16_contig", W.Workload("r1", n_h=128, batch=2, ctx=0, seed=41)),
+    ("bf16_paged", W.Workload("r2", n_h=128, batch=2, ctx=0, paged=True, seed=42)),
+    ("fp8", W.Workload("r3", n_h=128, batch=2, ctx=0, kv="fp8", seed=43)),
+    ("fp8_paged_h64", W.Workload("r4", n_h=64, batch=2, ctx=0, kv="fp8", paged=True, seed=44)),
+]
+
+
+@pytest.mark.parametrize("name,w", RESCALE, ids=[r[0] for r in RESCALE])
+@pytest.mark.parametrize("n_splits", [1, 3, 0])
+def test_running_max_rises_rescale_o(cuda_device, name, w, n_splits):
+    case = Case(w, cuda_device, lens=[3000, 2500], keep_rows=True)
+    _plant_spikes(case, SPIKES)
+    S = n_splits if n_splits else mla.num_splits(case.B, case.max_len, case.n_h)
+    events = sum(_count_rescales(case, b, S) for b in range(case.B))
+    # most heads rescale at every planted token after the first in a split
+    assert events >= case.n_h, f"the case triggers only {events} rescales"
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    out = case.run(n_splits=n_splits, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _compare(case, out, [(b, None) for b in range(case.B)])
+
+
+# ------------------------------------------------------------------------------------
+# Magnitudes. The e4m3 path works on f16 operands, so rows of very small or very large
+# magnitude (per-token scales from 2e-8 to 2e2) and queries whose absorbed form is far
+# above f16's maximum (65504) or below its normal range must not lose what matters.
+# Each sequence pairs a row factor with a query factor; their product keeps the scores'
+# spread at or below ~30 natural units, where the bf16 rounding of the absorbed query
+# (an error of ~1e-3 of the score's spread) cannot reorder the top tokens against the
+# exact oracle.
+# ------------------------------------------------------------------------------------
+MAGNITUDES = [   # (row factor, query factor); None = per-token factors 10^U(-3, 3)
+    (1e-3, 3e4), (1e-2, 3e3), (1e2, 0.3), (1e3, 0.03), (None, 0.03), (1.0, 30.0), (1e-5, 1e5), (1e5, 1e-5),
+]
+
+
+@pytest.mark.parametrize("kv,paged", [("fp8", False), ("fp8", True), ("bf16", False)])
+def test_row_and_query_magnitudes(cuda_device, kv, paged):
+    lens = [300, 257, 700, 129, 900, 450, 200, 333]
+    w = W.Workload("mag", n_h=128, batch=len(lens), ctx=0, kv=kv, paged=paged, seed=51)
+    case = Case(w, cuda_device, lens=lens, keep_rows=True)
+    rng = np.random.default_rng(5100)
+    for b, (f, _) in enumerate(MAGNITUDES):
+        L = lens[b]
+        fac = np.float32(f) if f is not None else (10.0 ** rng.uniform(-3, 3, (L, 1))).astype(np.float32)
+        case.set_rows(b, np.arange(L), W.f32_to_bf16_bits(rows_f32(case.rows_of(b)) * fac))
+    case.scale_queries([g for _, g in MAGNITUDES])
+    case.rebuild_cache()
+    for n_splits in (1, 3):
+        status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+        out = case.run(n_splits=n_splits, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for b in range(case.B):   # one sequence at a time: their outputs differ by 1e8 in size
+            _compare(case, out, [(b, None)])
+    if kv == "fp8":
+        for b in range(case.B):
+            _fp8_codes_match(case, b)
