@@ -155,8 +155,7 @@ __device__ __forceinline__ void convert_unit(const unsigned char* src, unsigned 
   *reinterpret_cast<uint4*>(dst_row + (((2 * c16 + 1) ^ (row & 7)) << 4)) = hi;
 }
 
-// 14 warps x 144 registers = 64,512 of the SM's 65,536 (the default cap of 128 spills)
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(144)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e4s_map,
                      const __grid_constant__ CUtensorMap e4v_map, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap omap, float scale_log2) {
@@ -348,7 +347,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
           const bool pos = sc_next > 0.f;
           sb[r] = sc_next;
           sb[128 + r] = pos ? __log2f(sc_next) : -INFINITY;
-          sb[256 + r] = pos ? 1.f / sc_next : 0.f;
+          sb[256 + r] = pos ? __frcp_rn(sc_next) : 0.f;
         }
         mbar_arrive(&bars[SB_SCLREADY + (i & 1)]);
         sc_next = row_scale(i + 1);

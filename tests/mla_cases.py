@@ -92,6 +92,25 @@ class Case(W.DeviceInputs):
                                           heads=heads)
 
 
+def lse_tolerance(case, b: int, heads) -> np.ndarray:
+    """Per-head bound on |lse_gpu - lse_oracle| from the one rounding the scores carry:
+    the absorbed query q_lat = [W_UK^T q^C ‖ RoPE(q^R)] is stored in bf16, an error of at
+    most half an ulp (2^-8 relative) per element, uniform and independent, so the error
+    of score s_t has std <= 2^-8/sqrt(3) · scale · ||q_lat ⊙ row_t||_2. The lse is a
+    softmax-weighted mean of score errors; six of those stds over the worst token bounds
+    it, plus 1e-4 for the fp32 normaliser and the exp2 approximation."""
+    rows = case.oracle_rows(b)
+    if rows.shape[0] == 0:
+        return np.zeros(len(heads))
+    q = rows_f32(case.q_bits[b]).astype(np.float64)
+    wk = rows_f32(case.wuk_bits).astype(np.float64)
+    hs = list(heads)
+    q_lat = np.concatenate([np.einsum("hd,hdj->hj", q[hs, :128], wk[hs]),
+                            mla_oracle.rope(q[hs, 128:], int(case.pos_np[b]))], axis=1)   # [h, 576]
+    norms = np.sqrt(np.einsum("hj,tj->ht", q_lat * q_lat, rows * rows)).max(axis=1)
+    return 6.0 * 2.0 ** -8 / np.sqrt(3.0) * mla_oracle.default_scale() * norms + 1e-4
+
+
 def tol_stats(got: np.ndarray, ref: np.ndarray) -> tuple[float, float]:
     err = np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))
     ref_abs = np.abs(np.asarray(ref, np.float64))

@@ -15,7 +15,7 @@ import torch
 
 import mla_latent_kv_69_b300 as mla
 import workloads as W
-from mla_cases import Case, assert_within_tolerance, rows_f32
+from mla_cases import Case, assert_within_tolerance, lse_tolerance, rows_f32
 from oracle import fp8_e4m3
 
 pytestmark = pytest.mark.gpu
@@ -32,9 +32,10 @@ def _compare(case, out, samples, check_lat=True):
         got.append(o[b, hs]); ref.append(r["o"][hs])
         got_lat.append(o_lat[b, hs]); ref_lat.append(r["o_lat"][hs])
         if case.lens[b] > 0:
-            # lse carries the score error of the bf16 query (2^-9 relative per element),
-            # which grows with the scores' magnitude; the fp32 normaliser adds ~1e-6
-            np.testing.assert_allclose(lse[b, hs], r["lse"][hs], atol=4e-3, rtol=2e-3)
+            err = np.abs(lse[b, hs] - r["lse"][hs])
+            tol = lse_tolerance(case, b, hs)
+            assert np.all(err <= tol), f"lse of sequence {b}: worst error {err.max():.3e}, " \
+                                       f"error/bound up to {np.max(err / tol):.2f}"
         else:
             assert np.all(np.isneginf(lse[b, hs]))
     got, ref = np.concatenate([g.ravel() for g in got]), np.concatenate([r.ravel() for r in ref])
@@ -242,8 +243,9 @@ def test_running_max_rises_rescale_o(cuda_device, name, w, n_splits):
     _plant_spikes(case, SPIKES)
     S = n_splits if n_splits else mla.num_splits(case.B, case.max_len, case.n_h)
     events = sum(_count_rescales(case, b, S) for b in range(case.B))
-    # most heads rescale at every planted token after the first in a split
-    assert events >= case.n_h, f"the case triggers only {events} rescales"
+    if n_splits:   # the automatic split count leaves about two tiles per split: no later tile can rise
+        # most heads rescale at every planted token after the first in a split
+        assert events >= case.n_h, f"the case triggers only {events} rescales"
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     out = case.run(n_splits=n_splits, status=status)
     torch.cuda.synchronize()
