@@ -191,6 +191,7 @@ def workload_config(w: W.Workload, lens, n_splits: int) -> dict:
     return {"workload": w.name, "n_h": w.n_h, "batch_per_gpu": w.batch, "ctx": int(np.max(lens)),
             "tokens_per_gpu": int(np.sum(lens, dtype=np.int64)), "kv": w.kv,
             "layout": "paged-64" if w.paged else "contiguous", "n_splits": int(n_splits),
+            "schedule": "library default (num_splits = 0): slots per sequence = n_splits",
             "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read; both outside the timed "
                   "intervals); the cache of every workload but the tiny one is also larger than L2"}
 
@@ -260,7 +261,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     else:
         cache = mla.Cache(case.source, None, case.block_table)
     B, n_h = case.B, case.n_h
-    S = mla.num_splits(B, case.max_len, n_h)
+    S = mla.num_splits(B, case.max_len, n_h)   # slots of the library's own schedule (n_splits = 0)
     bufs = dict(
         q_lat=torch.empty(B, n_h, 576, dtype=torch.bfloat16, device=dev),
         o_part=torch.empty(B, S, n_h, 512, dtype=torch.float32, device=dev),
@@ -289,7 +290,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         if i == 0:
             mla.absorb_q(case.q, case.w_uk, case.pos, q_lat=bufs["q_lat"])
         elif i == 1:
-            mla.decode_fwd(bufs["q_lat"], cache, case.seq_lens, case.max_len, n_splits=S,
+            mla.decode_fwd(bufs["q_lat"], cache, case.seq_lens, case.max_len, n_splits=0,
                            o_part=bufs["o_part"], lse_part=bufs["lse_part"])
         elif i == 2:
             mla.combine(bufs["o_part"], bufs["lse_part"], o_lat=bufs["o_lat"], lse=bufs["lse"])
@@ -377,7 +378,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         d_q.copy_(h_q, non_blocking=True)
         d_pos.copy_(h_pos, non_blocking=True)
         d_len.copy_(h_len, non_blocking=True)
-        mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=S, bufs=e2e_bufs)
+        mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=0, bufs=e2e_bufs)
         h_o.copy_(e2e_bufs["o"], non_blocking=True)
 
     for _ in range(max(args.warmup, 1)):

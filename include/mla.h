@@ -126,12 +126,19 @@ MLA_API mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* 
  *   cache      host pointer to the cache view above
  *   seq_lens   [B] int32 device, 0 <= L_b <= max_seq_len
  *   max_seq_len host upper bound of seq_lens (sizes the launch)
- *   num_splits S, 1..MLA_MAX_SPLITS, or 0 for mla_num_splits(B, max_seq_len, n_h)
- *   o_part     [B, S, n_h, 512] fp32 out, normalised per split
- *   lse_part   [B, S, n_h] fp32 out, natural-log normaliser of the split
- *              (-inf, with o_part = 0, for a split that holds no token)
+ *   num_splits S, 1..MLA_MAX_SPLITS: uniform splits; or 0: the library's schedule
+ *              with S = mla_num_splits(B, max_seq_len, n_h) slots per sequence
+ *   o_part     [B, S, n_h, 512] fp32 out, normalised per slot
+ *   lse_part   [B, S, n_h] fp32 out, natural-log normaliser of the slot
  *   status     optional device int32 (may be NULL)
- *   Split s of sequence b covers the tokens mla_split_range(L_b, S, s) returns.
+ *   Uniform splits (num_splits >= 1): slot s of sequence b covers the tokens
+ *   mla_split_range(L_b, S, s) returns; a slot without tokens gets lse = -inf, o = 0.
+ *   Library schedule (num_splits = 0): for a bf16 cache the batch's 128-token tiles,
+ *   sequence after sequence, are shared out evenly among the GPU's SM pairs; each
+ *   sequence is cut into at most S pieces (one per slot, in token order); slots a
+ *   sequence does not use get lse = -inf and their o_part is left as it was. For an
+ *   e4m3 cache the schedule is uniform splits over the first slots. Either way
+ *   mla_combine over the S slots gives the whole-sequence result.
  *   A cache of 2^31 - 256 rows or more returns MLA_ERR_UNSUPPORTED (32-bit TMA rows).
  */
 MLA_API mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache,
@@ -191,7 +198,7 @@ MLA_API mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t*
  *   array's device address up (cudaGetSymbolAddress) and should come before any stream
  *   capture. Allocates nothing.
  */
-#define MLA_STATIC_SCRATCH_BYTES (32 << 20)
+#define MLA_STATIC_SCRATCH_BYTES (64 << 20)
 MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens,
                                              int B, int n_h, int max_seq_len, float softmax_scale, int num_splits,
                                              float* o_lat, float* lse, int32_t* status, cudaStream_t stream);
@@ -206,7 +213,8 @@ MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache*
  * (-1 for an invalid combination). Host only. */
 MLA_API int mla_decode_kernel(int kv_dtype, int n_h);
 
-/* Split count num_splits = 0 resolves to (>= 1, <= MLA_MAX_SPLITS). Host only. */
+/* Slots per sequence that num_splits = 0 uses (>= 1, <= MLA_MAX_SPLITS): the o_part /
+ * lse_part sizes to allocate for it. Host only. */
 MLA_API int mla_num_splits(int B, int max_seq_len, int n_h);
 
 /*

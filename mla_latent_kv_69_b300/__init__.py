@@ -202,8 +202,9 @@ def decode_fwd(q_lat, cache: Cache, seq_lens, max_seq_len: int, softmax_scale: f
     dev = _one_device(q_lat=q_lat, seq_lens=seq_lens, o_part=o_part, lse_part=lse_part, status=status,
                       **cache.tensors())
     scale = default_scale() if softmax_scale is None else float(softmax_scale)
-    _call("mla_decode_fwd", dev, _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale, S,
-          _ptr(o_part), _ptr(lse_part), _ptr(status), stream=stream)
+    # n_splits = 0 keeps the library's own schedule (o_part then has S = num_splits() slots)
+    _call("mla_decode_fwd", dev, _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len), scale,
+          int(n_splits) if n_splits > 0 else 0, _ptr(o_part), _ptr(lse_part), _ptr(status), stream=stream)
     return o_part, lse_part
 
 

@@ -21,7 +21,7 @@ MLA_ERR_DEVICE_BOUNDS = 6
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
 MLA_MAX_SPLITS = 256
-MLA_STATIC_SCRATCH_BYTES = 32 << 20
+MLA_STATIC_SCRATCH_BYTES = 64 << 20
 
 EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",

@@ -54,7 +54,10 @@ struct DecodeParams {
   int64_t num_rows;             // addressable rows
   int32_t max_pages;
   int32_t kv_dtype;             // mla_kv_dtype
-  int32_t B, n_h, S;
+  int32_t B, n_h, S;            // S: partial-result slots per sequence (the row stride of o_part)
+  int32_t S_used;               // uniform schedule: splits per sequence (<= S)
+  int32_t balanced;             // 1: balanced schedule over `pairs` SM pairs; 0: one pair per (b, split)
+  int32_t pairs;                // balanced schedule: SM pairs sharing the batch
   float scale;                  // softmax scale (natural-log units)
 };
 

@@ -67,13 +67,198 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// ------------------------------ work schedule ----------------------------------------
+// A decode launch assigns the batch's tokens to SM pairs (2-CTA clusters) in pieces; each
+// piece is one contiguous token range of one sequence and writes one partial-result slot.
+//   uniform  (balanced = 0): pair (b, s) takes split s of S_used uniform splits of b
+//            (mla_split_range), slot s; the pair of split S_used - 1 marks the slots
+//            S_used .. S - 1 unused.
+//   balanced (balanced = 1): the batch's 128-token tiles are laid end to end (sequence
+//            by sequence) and pair p takes tiles [p q, (p + 1) q). The quota q is at least
+//            ceil(T / pairs) (every pair busy) and, unless S covers the longest sequence
+//            tile by tile, at least ceil(T_max / (S - 1)), so that no sequence is cut into
+//            more than S pieces. A piece's slot is the index of its pair minus the index
+//            of the pair holding the sequence's first tile; the pair holding its last tile
+//            marks the later slots unused, and empty sequences are marked by pair b % pairs.
+constexpr int kSchedTile = 128;
+
+struct Piece {
+  int b, st, en;   // sequence and token range [st, en)
+  int slot;        // partial-result slot of sequence b
+  int fill_from;   // slots fill_from .. S - 1 of b are unused and get lse = -inf (S: none)
+};
+
+struct SchedShared {   // the pair's share, computed once per CTA by sched_init
+  int64_t c0;          // global index of the first tile of sequence b0
+  int64_t t_begin, t_end, q;
+  int32_t b0;
+  int32_t pad;
+};
+
+// Tiles per pair for T tiles in all, the longest sequence T_max tiles long, S slots per
+// sequence and `pairs` SM pairs. A piece holds at least one tile, so S >= T_max needs no
+// bound; otherwise the quota keeps every sequence within S pieces (with S == 1: one pair
+// takes everything).
+__host__ __device__ inline int64_t sched_quota(int64_t T, int Tmax, int S, int pairs) {
+  int64_t q = (T + pairs - 1) / pairs;
+  if (S < Tmax) {
+    const int64_t qmin = S >= 2 ? (Tmax + S - 2) / (S - 1) : (T > 0 ? T : 1);
+    q = q > qmin ? q : qmin;
+  }
+  return q < 1 ? 1 : q;
+}
+
+// Block-wide: every thread of the CTA calls it with the same arguments. `scratch` holds
+// 12 bytes per thread and is free for the call's duration; the result lands in `out`
+// (visible to all threads on return).
+__device__ inline void sched_init(const DecodeParams& p, int pair, unsigned char* scratch, SchedShared* out) {
+  const int nthr = blockDim.x, tid = threadIdx.x;
+  if (!p.balanced) {
+    __syncthreads();
+    return;
+  }
+  int64_t* sums = reinterpret_cast<int64_t*>(scratch);
+  int* maxs = reinterpret_cast<int*>(scratch + 8 * nthr);
+  const int K = (p.B + nthr - 1) / nthr;
+  const int lo = min(p.B, tid * K), hi = min(p.B, lo + K);
+  int64_t sum = 0;
+  int mx = 0;
+  for (int b = lo; b < hi; ++b) {
+    const int T = (max(p.seq_lens[b], 0) + kSchedTile - 1) / kSchedTile;
+    sum += T;
+    mx = max(mx, T);
+  }
+  sums[tid] = sum;
+  maxs[tid] = mx;
+  __syncthreads();
+  if (tid < 32) {   // exclusive prefix over the per-thread sums, total and maximum
+    const int E = (nthr + 31) / 32;
+    int64_t run = 0;
+    int m = 0;
+    for (int i = tid * E; i < min(nthr, tid * E + E); ++i) {
+      const int64_t v = sums[i];
+      sums[i] = run;
+      run += v;
+      m = max(m, maxs[i]);
+    }
+    int64_t incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid >= off) incl += o;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const int64_t excl = incl - run;
+    for (int i = tid * E; i < min(nthr, tid * E + E); ++i) sums[i] += excl;
+    if (tid == 31) {
+      const int64_t T = incl;
+      const int64_t q = sched_quota(T, m, p.S, p.pairs);
+      out->q = q;
+      out->t_begin = (int64_t)pair * q;
+      out->t_end = min((int64_t)(pair + 1) * q, T);
+      out->b0 = -1;
+      out->c0 = 0;
+    }
+  }
+  __syncthreads();
+  const int64_t tb = out->t_begin;
+  const int64_t ex = sums[tid];
+  if (tb < out->t_end && ex <= tb && tb < ex + sum) {
+    int64_t c = ex;
+    for (int b = lo; b < hi; ++b) {
+      const int T = (max(p.seq_lens[b], 0) + kSchedTile - 1) / kSchedTile;
+      if (tb < c + T) {
+        out->b0 = b;
+        out->c0 = c;
+        break;
+      }
+      c += T;
+    }
+  }
+  __syncthreads();
+}
+
+// Walks the pieces of one pair in order; every role of both CTAs walks the same list.
+struct PieceCursor {
+  int64_t cb, tile, end, q;
+  int b;
+  bool done;
+
+  __host__ __device__ void start(const DecodeParams& p, int pair, const SchedShared& sh) {
+    if (p.balanced) {
+      b = sh.b0;
+      cb = sh.c0;
+      tile = sh.t_begin;
+      end = sh.b0 >= 0 ? sh.t_end : sh.t_begin;
+      q = sh.q;
+      done = false;
+    } else {
+      b = pair / p.S_used;
+      tile = pair % p.S_used;   // the split index
+      done = false;
+    }
+  }
+
+  __host__ __device__ bool next(const DecodeParams& p, Piece& pc) {
+    if (!p.balanced) {
+      if (done) return false;
+      done = true;
+      const int L = p.seq_lens[b] > 0 ? p.seq_lens[b] : 0;
+      pc.b = b;
+      pc.slot = (int)tile;
+      split_range(L, p.S_used, pc.slot, &pc.st, &pc.en);
+      pc.fill_from = pc.slot == p.S_used - 1 ? p.S_used : p.S;
+      return true;
+    }
+    while (tile < end && b < p.B) {
+      const int L = p.seq_lens[b] > 0 ? p.seq_lens[b] : 0;
+      const int64_t Tb = (L + kSchedTile - 1) / kSchedTile;
+      if (tile >= cb + Tb) {
+        cb += Tb;
+        ++b;
+        continue;
+      }
+      const int64_t seg_end = end < cb + Tb ? end : cb + Tb;
+      pc.b = b;
+      pc.st = (int)((tile - cb) * kSchedTile);
+      pc.en = (int)((seg_end - cb) * kSchedTile < L ? (seg_end - cb) * kSchedTile : L);
+      pc.slot = (int)(tile / q - cb / q);
+      pc.fill_from = seg_end == cb + Tb ? pc.slot + 1 : p.S;
+      tile = seg_end;
+      if (pc.slot >= p.S) {   // only if seq_lens changed under the launch: stop, consistently in every role
+#ifdef __CUDA_ARCH__
+        record_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+#endif
+        tile = end;
+        return false;
+      }
+      return true;
+    }
+    return false;
+  }
+};
+
+// Balanced schedule: lse = -inf in every slot of the empty sequences b = pair (mod
+// pairs), written by threads tid0, tid0 + nthr, ... (o_part is never read for such
+// slots). Call it only after the previous kernel of the stream is complete.
+__device__ inline void mark_empty_sequences(const DecodeParams& p, int pair, int tid0, int nthr) {
+  if (!p.balanced) return;
+  for (int b = pair; b < p.B; b += p.pairs) {
+    if (p.seq_lens[b] > 0) continue;
+    for (int i = tid0; i < p.S * p.n_h; i += nthr) p.lse_part[(int64_t)b * p.S * p.n_h + i] = -INFINITY;
+  }
+}
+
 // True when the tcgen05 kernels handle this configuration.
 bool decode_tc_supported(const DecodeParams& p);
 // e4m3 cache: tcgen05 kernel with f16 operands (decode_tc_fp8.cu).
 cudaError_t launch_decode_tc_fp8(const DecodeParams& p, cudaStream_t st);
 // Launch; max_seq_len sizes nothing on the device side but is kept for heuristics.
 cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_t st);
-// Split count for B sequences of up to `tiles` 64-token tiles.
+// Uniform split count for B sequences of up to `tiles` 64-token tiles.
 int decode_tc_num_splits(int B, int tiles, int n_h, int sms);
+// Slots per sequence of the balanced schedule (what num_splits = 0 resolves to).
+int decode_balanced_slots(int B, int max_seq_len, int pairs);
 
 }  // namespace mla

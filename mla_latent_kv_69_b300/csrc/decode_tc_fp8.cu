@@ -164,10 +164,12 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
   const uint32_t peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x >> 1;
-  const int b = unit / p.S, s = unit % p.S;
+  // uniform schedule: split s of S_used, written to slot s of S (slots S_used .. S - 1
+  // are marked unused by the last split)
+  const int b = unit / p.S_used, s = unit % p.S_used;
   const int L = max(p.seq_lens[b], 0);
   int st, en;
-  split_range(L, p.S, s, &st, &en);
+  split_range(L, p.S_used, s, &st, &en);
   const int n_tiles = (en - st + kTile - 1) / kTile;
   const int n_halves = 2 * n_tiles;
   griddep_launch_dependents();
@@ -178,8 +180,10 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       float* o = p.o_part + ((int64_t)b * p.S + s) * p.n_h * kLatent;
       for (int i = threadIdx.x; i < p.n_h * kLatent / 4; i += kThreads)
         reinterpret_cast<float4*>(o)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int h = threadIdx.x; h < p.n_h; h += kThreads)
-        p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] = -INFINITY;
+      const int from = s == p.S_used - 1 ? s : p.S;   // this slot and the unused ones after it
+      for (int i = threadIdx.x; i < p.n_h; i += kThreads) p.lse_part[((int64_t)b * p.S + s) * p.n_h + i] = -INFINITY;
+      for (int i = threadIdx.x; i < (p.S - from - 1) * p.n_h && from < p.S; i += kThreads)
+        p.lse_part[((int64_t)b * p.S + from + 1) * p.n_h + i] = -INFINITY;
     }
     return;
   }
@@ -759,6 +763,9 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       if (j == 0 && h < p.n_h)
         p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] =
             good ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      if (s == p.S_used - 1)   // slots after the last split are unused
+        for (int i = threadIdx.x - 64; i < (p.S - p.S_used) * p.n_h; i += 256)
+          p.lse_part[((int64_t)b * p.S + p.S_used) * p.n_h + i] = -INFINITY;
       tc_fence_before();
     }
   }
@@ -839,7 +846,7 @@ cudaError_t launch_decode_tc_fp8(const DecodeParams& p, cudaStream_t st) {
   if (attr_err != cudaSuccess) return attr_err;
   // 2^8: the f16 operands hold 2^-8 times the codes' values
   const float scale_log2 = p.scale * 1.4426950408889634f * 256.f;
-  const int64_t ctas = 2ll * p.B * p.S;
+  const int64_t ctas = 2ll * p.B * p.S_used;
   return launch_overlapped(decode_tc_fp8_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmemBytes, st, p, e4s, e4v,
                            qmap, omap, scale_log2);
 }

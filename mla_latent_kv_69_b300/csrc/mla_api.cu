@@ -78,9 +78,7 @@ int mla_decode_kernel(int kv_dtype, int n_h) {
 
 int mla_num_splits(int B, int max_seq_len, int n_h) {
   if (B < 1 || max_seq_len < 0 || !valid_heads(n_h)) return 1;
-  const int tiles = ceil_div(max_seq_len, kPage);
-  if (tiles <= 1) return 1;
-  return decode_tc_num_splits(B, tiles, n_h, sm_count());
+  return decode_balanced_slots(B, max_seq_len, sm_count() / 2);
 }
 
 mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* pos, int B, int n_h,
@@ -144,6 +142,19 @@ mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32
   p.B = B;
   p.n_h = n_h;
   p.S = S;
+  p.S_used = S;
+  p.balanced = 0;
+  p.pairs = 0;
+  if (num_splits == 0) {
+    if (cache->dtype == MLA_KV_BF16) {   // the persistent kernel shares the batch out evenly
+      p.balanced = 1;
+      p.pairs = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+    } else {                             // uniform splits within the slots
+      const int tiles = ceil_div(max_seq_len, kPage);
+      const int su = tiles <= 1 ? 1 : decode_tc_num_splits(B, tiles, n_h, sm_count());
+      p.S_used = su < S ? su : S;
+    }
+  }
   p.scale = softmax_scale;
   // TMA coordinates are 32-bit: a cache of 2^31 rows (over 1 TB) is not served.
   if (!decode_tc_supported(p)) return MLA_ERR_UNSUPPORTED;

@@ -462,3 +462,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
 }
 }  // namespace sm100
 }  // namespace mla
+
+namespace mla {
+namespace sm100 {
+// Order this thread's earlier memory operations (including stores to a peer CTA's shared
+// memory) before its later ones, at cluster scope.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+__device__ __forceinline__ void st_cluster_v2_f32(uint32_t caddr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(caddr), "f"(a), "f"(b) : "memory");
+}
+}  // namespace sm100
+}  // namespace mla

@@ -106,10 +106,11 @@ mla_status mla_decode_combine_static(const void* q_lat, const mla_cache* cache, 
   if (!scratch) return MLA_ERR_CUDA;
   float* o_part = reinterpret_cast<float*>(scratch);
   float* lse_part = reinterpret_cast<float*>(scratch + part_bytes);
-  // Every (sequence, split, head) entry is written by the decode before the merge
-  // reads it (empty splits write 0 and -inf), so nothing needs clearing.
-  const mla_status st = mla_decode_fwd(q_lat, cache, seq_lens, B, n_h, max_seq_len, softmax_scale, S, o_part,
-                                       lse_part, status, stream);
+  // Every (sequence, slot, head) lse entry is written by the decode before the merge
+  // reads it (-inf for a slot without tokens, whose o_part the merge skips), so nothing
+  // needs clearing.
+  const mla_status st = mla_decode_fwd(q_lat, cache, seq_lens, B, n_h, max_seq_len, softmax_scale, num_splits,
+                                       o_part, lse_part, status, stream);
   if (st != MLA_OK) return st;
   return mla_combine(o_part, lse_part, B, S, n_h, o_lat, lse, stream);
 }
