@@ -161,6 +161,30 @@ def attend_absorbed(q, c_kv, k_rope, w_uk, w_uv, pos_q, scale=None, base: float 
     return dict(o=o, lse=lse, o_lat=o_lat)
 
 
+def attend_latent(q_lat, rows, scale=None):
+    """Attention of the absorbed query over the cached rows, what the decode and merge
+    calls compute from a given absorbed query ([A] §"长上下文推理的第一瓶颈": with W_UK
+    folded into the query every head attends directly over the cached latent; the
+    decoupled RoPE key is the rows' last 64 columns, [A] §"解耦 RoPE 与 YaRN").
+
+    q_lat   [n_h, 576]  absorbed query: W_UK[h]^T q^C ‖ RoPE(q^R) per head
+    rows    [L, 576]    cached rows c_KV ‖ k^R
+    Returns dict with o_lat [n_h, 512] = sum_t p_t c_t and lse [n_h].
+    """
+    q_lat = _f64(q_lat)
+    rows = _f64(rows)
+    n_h = q_lat.shape[0]
+    scale = default_scale() if scale is None else float(scale)
+    if rows.shape[0] == 0:
+        return dict(o_lat=np.zeros((n_h, D_C)), lse=np.full(n_h, -np.inf))
+    s = (q_lat @ rows.T) * scale                          # [n_h, L]
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    z = e.sum(axis=1)
+    p = e / z[:, None]
+    return dict(o_lat=p @ rows[:, :D_C], lse=m + np.log(z))
+
+
 # ---------------------------------------------------------------------------------
 # Log-sum-exp merge of attention over disjoint token subsets. The exact identity:
 # for a partition of the tokens into parts j with normalised outputs o_j and

@@ -82,6 +82,34 @@ def test_absorbed_matches_explicit_bruteforce_sizes():
             np.testing.assert_allclose(a[k], b[k], rtol=1e-12, atol=1e-13)
 
 
+def test_latent_form_matches_explicit_bruteforce_sizes():
+    # the absorbed query built by hand reproduces the explicit form's o_lat and lse
+    rng = np.random.default_rng(41)
+    for n_h, L, pos in [(1, 1, 0), (2, 3, 2), (4, 8, 100), (3, 5, 131071)]:
+        q, c, kr, wk, wv = _rand_case(rng, n_h=n_h, L=L)
+        a = M.attend_explicit(q, c, kr, wk, wv, pos_q=pos)
+        q_lat = np.concatenate([np.einsum("hd,hdj->hj", q[:, :128], wk), M.rope(q[:, 128:], pos)], axis=1)
+        b = M.attend_latent(q_lat, np.concatenate([c, kr], axis=1))
+        np.testing.assert_allclose(b["o_lat"], a["o_lat"], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(b["lse"], a["lse"], rtol=1e-12, atol=1e-13)
+
+
+def test_latent_form_scalar_bruteforce():
+    rng = np.random.default_rng(42)
+    q_lat = rng.standard_normal((2, 576)) * 3.0
+    rows = rng.standard_normal((4, 576))
+    r = M.attend_latent(q_lat, rows)
+    scale = 1.0 / math.sqrt(192.0)
+    for h in range(2):
+        s = [sum(q_lat[h, d] * rows[t, d] for d in range(576)) * scale for t in range(4)]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        z = sum(e)
+        for j in (0, 7, 300, 511):
+            assert r["o_lat"][h, j] == pytest.approx(sum(e[t] / z * rows[t, j] for t in range(4)), rel=1e-12, abs=1e-14)
+        assert r["lse"][h] == pytest.approx(m + math.log(z), rel=1e-13)
+
+
 def _scalar_loop_attention(q, c, kr, wk, wv, pos_q, scale):
     """Brute force with Python scalars only (no NumPy linear algebra)."""
     n_h, L = q.shape[0], c.shape[0]

@@ -63,6 +63,13 @@ ORACLE_MUTANTS = [
     ("attend_explicit", "o_lat[h] = p @ c", "o_lat[h] = e @ c"),
     ("attend_explicit", "lse[h] = m + math.log(z)", "lse[h] = m + math.log2(z)"),
     ("attend_explicit", "qh = np.concatenate([q[h, :D_H], q_r[h]])", "qh = np.concatenate([q[h, :D_H], q[h, D_H:]])"),
+    # latent form: the scale, the RoPE key columns, the value columns, the log base
+    ("attend_latent", "s = (q_lat @ rows.T) * scale", "s = q_lat @ rows.T"),
+    ("attend_latent", "s = (q_lat @ rows.T) * scale", "s = (q_lat[:, :D_C] @ rows[:, :D_C].T) * scale"),
+    ("attend_latent", "return dict(o_lat=p @ rows[:, :D_C], lse=m + np.log(z))",
+     "return dict(o_lat=p @ rows[:, D_R:], lse=m + np.log(z))"),
+    ("attend_latent", "return dict(o_lat=p @ rows[:, :D_C], lse=m + np.log(z))",
+     "return dict(o_lat=p @ rows[:, :D_C], lse=m + np.log2(z))"),
     # split merge
     ("merge_partials", "np.exp(lse_parts - m_safe)", "np.exp(m_safe - lse_parts)"),
     ("merge_partials", "o = np.where(finite[..., None], o / np.where(finite, z, 1.0)[..., None], 0.0)",

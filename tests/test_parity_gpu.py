@@ -15,8 +15,8 @@ import torch
 
 import mla_latent_kv_69_b300 as mla
 import workloads as W
-from mla_cases import Case, assert_within_tolerance, lse_tolerance, rows_f32
-from oracle import fp8_e4m3
+from mla_cases import Case, assert_within_tolerance, bits_to_torch_bf16, lse_tolerance, rows_f32
+from oracle import fp8_e4m3, mla_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -255,21 +255,22 @@ def test_running_max_rises_rescale_o(cuda_device, name, w, n_splits):
 
 # ------------------------------------------------------------------------------------
 # Magnitudes. The e4m3 path works on f16 operands, so rows of very small or very large
-# magnitude (per-token scales from 2e-8 to 2e2) and queries whose absorbed form is far
-# above f16's maximum (65504) or below its normal range must not lose what matters.
-# Each sequence pairs a row factor with a query factor; their product keeps the scores'
-# spread at or below ~30 natural units, where the bf16 rounding of the absorbed query
-# (an error of ~1e-3 of the score's spread) cannot reorder the top tokens against the
-# exact oracle.
+# magnitude (per-token scales from 2e-8 to 2e2) and absorbed queries far above f16's
+# maximum (65504) or below its normal range must not lose what matters. The decode and
+# merge calls are fed a query drawn directly (bf16) and compared with the oracle's
+# latent form on the same query; going through the absorption step instead would add the
+# bf16 rounding of the absorbed query, whose effect on the scores grows with their spread
+# (at a spread of ~30 natural units it alone reaches the tolerance, for any kernel).
 # ------------------------------------------------------------------------------------
-MAGNITUDES = [   # (row factor, query factor); None = per-token factors 10^U(-3, 3)
-    (1e-3, 3e4), (1e-2, 3e3), (1e2, 0.3), (1e3, 0.03), (None, 0.03), (1.0, 30.0), (1e-5, 1e5), (1e5, 1e-5),
+MAGNITUDES = [   # (row factor, absorbed-query factor); None = per-token factors 10^U(-3, 3)
+    (1e-3, 3e3), (1e-2, 500.0), (1e2, 0.05), (1e3, 0.005), (None, 0.005), (1.0, 30.0), (1e-5, 1e5), (1e5, 1e-5),
+    (1.0, 1e3),
 ]
 
 
-@pytest.mark.parametrize("kv,paged", [("fp8", False), ("fp8", True), ("bf16", False)])
+@pytest.mark.parametrize("kv,paged", [("fp8", False), ("fp8", True), ("bf16", False), ("bf16", True)])
 def test_row_and_query_magnitudes(cuda_device, kv, paged):
-    lens = [300, 257, 700, 129, 900, 450, 200, 333]
+    lens = [300, 257, 700, 129, 900, 450, 200, 333, 520]
     w = W.Workload("mag", n_h=128, batch=len(lens), ctx=0, kv=kv, paged=paged, seed=51)
     case = Case(w, cuda_device, lens=lens, keep_rows=True)
     rng = np.random.default_rng(5100)
@@ -277,15 +278,23 @@ def test_row_and_query_magnitudes(cuda_device, kv, paged):
         L = lens[b]
         fac = np.float32(f) if f is not None else (10.0 ** rng.uniform(-3, 3, (L, 1))).astype(np.float32)
         case.set_rows(b, np.arange(L), W.f32_to_bf16_bits(rows_f32(case.rows_of(b)) * fac))
-    case.scale_queries([g for _, g in MAGNITUDES])
     case.rebuild_cache()
-    for n_splits in (1, 3):
+    q_lat_bits = W.f32_to_bf16_bits(rows_f32(W.gen_q_lat(w)) * np.array([g for _, g in MAGNITUDES], np.float32)[:, None, None])
+    q_lat = bits_to_torch_bf16(q_lat_bits, cuda_device)
+    q64 = rows_f32(q_lat_bits).astype(np.float64)
+    for n_splits in (1, 3, 0):
         status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-        out = case.run(n_splits=n_splits, status=status)
+        o_part, lse_part = mla.decode_fwd(q_lat, case.cache, case.seq_lens, case.max_len, n_splits=n_splits,
+                                          status=status)
+        o_lat, lse = mla.combine(o_part, lse_part)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
+        o_lat, lse = o_lat.double().cpu().numpy(), lse.double().cpu().numpy()
         for b in range(case.B):   # one sequence at a time: their outputs differ by 1e8 in size
-            _compare(case, out, [(b, None)])
+            ref = mla_oracle.attend_latent(q64[b], case.oracle_rows(b))
+            assert_within_tolerance(o_lat[b], ref["o_lat"], f"o_lat, sequence {b}")
+            # the query is exact here: the fp32 scores and normaliser leave ~1e-6 relative
+            np.testing.assert_allclose(lse[b], ref["lse"], rtol=2e-5, atol=2e-4)
     if kv == "fp8":
         for b in range(case.B):
             _fp8_codes_match(case, b)

@@ -36,7 +36,7 @@ D_ROW = 576
 D_Q = 192
 PAGE = 64
 
-TAG_Q, TAG_ROWS, TAG_WUK, TAG_WUV, TAG_LENS, TAG_PAGES = 1, 2, 3, 4, 5, 6
+TAG_Q, TAG_ROWS, TAG_WUK, TAG_WUV, TAG_LENS, TAG_PAGES, TAG_QLAT = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclass(frozen=True)
@@ -107,6 +107,12 @@ def seq_lens(w: Workload) -> np.ndarray:
 def gen_q(w: Workload) -> np.ndarray:
     """bf16 bits [B, n_h, 192]."""
     return _normal_bf16(stream(w.seed, TAG_Q), (w.batch, w.n_h, D_Q))
+
+
+def gen_q_lat(w: Workload) -> np.ndarray:
+    """bf16 bits [B, n_h, 576], N(0, 1): an absorbed query drawn directly, for feeding the
+    decode call without the absorption step."""
+    return _normal_bf16(stream(w.seed, TAG_QLAT), (w.batch, w.n_h, D_ROW))
 
 
 def gen_w_uk(w: Workload) -> np.ndarray:
