@@ -133,12 +133,14 @@ MLA_API mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* 
  *   status     optional device int32 (may be NULL)
  *   Uniform splits (num_splits >= 1): slot s of sequence b covers the tokens
  *   mla_split_range(L_b, S, s) returns; a slot without tokens gets lse = -inf, o = 0.
- *   Library schedule (num_splits = 0): for a bf16 cache the batch's 128-token tiles,
- *   sequence after sequence, are shared out evenly among the GPU's SM pairs; each
- *   sequence is cut into at most S pieces (one per slot, in token order); slots a
- *   sequence does not use get lse = -inf and their o_part is left as it was. For an
- *   e4m3 cache the schedule is uniform splits over the first slots. Either way
- *   mla_combine over the S slots gives the whole-sequence result.
+ *   Library schedule (num_splits = 0): for a paged bf16 cache the batch's 128-token
+ *   tiles, sequence after sequence, are shared out evenly among the GPU's SM pairs
+ *   (or, when every sequence has the same tile count and that is cheaper, each
+ *   sequence is cut into equal pieces); each sequence is cut into at most S pieces
+ *   (one per slot, in token order); slots a sequence does not use get lse = -inf and
+ *   their o_part is left as it was. For a contiguous cache and for an e4m3 cache the
+ *   schedule is uniform splits, sized for max_seq_len, over the first slots. Either
+ *   way mla_combine over the S slots gives the whole-sequence result.
  *   A cache of 2^31 - 256 rows or more returns MLA_ERR_UNSUPPORTED (32-bit TMA rows).
  */
 MLA_API mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache,

@@ -116,7 +116,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(S_PANEL % 1024 == 0 && V_PANEL % 1024 == 0 && kGroup % 1024 == 0, "swizzle alignment");
 static_assert(OFF_SCHED % 8 == 0 && V_FIN % 16 == 0, "alignment");
 static_assert(8 * kEpiBuf * 2 <= kCStage, "epilogue staging fits in one value stage");
-static_assert(12 * kThreads <= kRing * kGroup, "schedule scratch fits in the ring");
+static_assert(8 * kEpiBuf * 6 <= kCStages * kCStage, "last epilogue staging fits in the value stages");
+static_assert(16 * kThreads <= kRing * kGroup, "schedule scratch fits in the ring");
 
 // Row-warp commands (the piece index travels in bits 8 and up for CMD_EPI)
 enum Cmd { CMD_ZERO = 1, CMD_RESCALE = 2, CMD_EPI = 4, CMD_EXIT = 8 };
@@ -141,6 +142,8 @@ __device__ __forceinline__ void fill_unused_slots(const DecodeParams& p, int b, 
     p.lse_part[part_row(p, b, from) + i] = -INFINITY;
 }
 
+// kMulti = false: one piece per pair (the uniform schedule), the piece walk compiled out.
+template <bool kMulti>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
@@ -160,9 +163,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
   }
   // The pair's pieces (seq_lens is not written by the previous kernel of the step).
   SchedShared* sched = reinterpret_cast<SchedShared*>(smem + OFF_SCHED);
-  sched_init(p, pair, smem, sched);
+  if (kMulti) sched_init(p, pair, smem, sched);
   PieceCursor cur;
   cur.start(p, pair, *sched);
+  auto next_piece = [&](Piece& pc) -> bool { return kMulti && cur.next(p, pc); };
   Piece first;
   const bool any = cur.next(p, first);
   if (!any || first.en <= first.st) {
@@ -241,10 +245,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         prefetch_tmap(&smap);
         prefetch_tmap(&qmap);
         griddep_wait();   // q_lat comes from the previous kernel
-        int64_t k = 0;
+        uint32_t k = 0;
         bool ok = true;
         Piece pc = first;
-        auto slot_ready = [&](int64_t item) -> bool {   // the slot's previous item was consumed
+        auto slot_ready = [&](uint32_t item) -> bool {   // the slot's previous item was consumed
           if (item < kRing) return true;
           return mbar_wait(&bars[SB_SLOT_EMPTY + (int)(item % kRing)], (uint32_t)(((item / kRing) - 1) & 1), abort_flag,
                            kWaitNs);
@@ -295,11 +299,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
               }
             }
           }
-        } while (ok && !*abort_flag && cur.next(p, pc));
+        } while (ok && !*abort_flag && next_piece(pc));
         if (!ok) give_up(p, abort_flag, smem, peer);
         // Loads still in flight land before the CTA may leave.
         const volatile int never = 0;
-        for (int64_t i = k > kRing ? k - kRing : 0; i < k; ++i)
+        for (uint32_t i = k > kRing ? k - kRing : 0; i < k; ++i)
           mbar_wait(&bars[SB_SLOT_FULL + (int)(i % kRing)], (uint32_t)((i / kRing) & 1), &never, kWaitNs / 4);
       }
     } else if (warp == 1) {
@@ -307,7 +311,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         // ---- S = Q · C^T, 36 MMAs of 128 x 128 x 16 per tile ----
         const uint32_t idq = idesc_f16(128, kTile, false, false, false);
         bool ok = true;
-        int64_t k = 0, tg = 0;   // ring item, tile of the pair
+        uint32_t k = 0, tg = 0;   // ring item, tile of the pair
         int np = 0;              // piece of the pair
         Piece pc = first;
         do {
@@ -344,7 +348,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             mma_commit(&bars[SB_SFULL]);
           }
           ++np;
-        } while (ok && cur.next(p, pc));
+        } while (ok && next_piece(pc));
         if (!ok) give_up(p, abort_flag, smem, peer);
         mma_commit(&bars[SB_FLUSH]);
         const volatile int never = 0;
@@ -360,7 +364,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       const uint32_t panel_remote = mapa(smem_u32(smem + V_PANEL + j * kPanel), 1);
       const uint32_t hdr_remote = mapa(smem_u32(smem + V_HDR), 1);
       const uint32_t pfull_remote = mapa(smem_u32(&bars[VB_PFULL + j]), 1);
-      int64_t k = 0, tg = 0;
+      uint32_t k = 0, tg = 0;
       int np = 0;
       Piece pc = first;
       // Every thread runs every iteration and every named barrier; after an abort the
@@ -505,7 +509,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         const uint32_t stop = named_popc(1, 256, *abort_flag != 0);
         ++np;
         if (stop) break;
-      } while (cur.next(p, pc));
+      } while (next_piece(pc));
     }
   } else {
     // =============================== value CTA =========================================
@@ -514,7 +518,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         // ---- TMA producer: c_KV of every 64-token step (evict-first: last reader) ----
         const uint64_t pol = l2_policy_evict_first();
         prefetch_tmap(&vmap);
-        int64_t u = 0;   // step of the pair
+        uint32_t u = 0;   // step of the pair
         int np = 0;
         bool ok = true;
         // The epilogue of piece n stages O in the stage of the piece's last step, s_n; a
@@ -559,11 +563,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
           if (!ok || *abort_flag) break;
           prev_stage = (int)((u - 1) % kCStages);   // where this piece's epilogue stages O
           ++np;
-          if (!cur.next(p, pc)) break;
+          if (!next_piece(pc)) break;
         }
         if (!ok) give_up(p, abort_flag, smem, peer);
         const volatile int never = 0;
-        for (int64_t i = u > kCStages ? u - kCStages : 0; i < u; ++i)
+        for (uint32_t i = u > kCStages ? u - kCStages : 0; i < u; ++i)
           mbar_wait(&bars[VB_CFULL + (int)(i % kCStages)], (uint32_t)((i / kCStages) & 1), &never, kWaitNs / 4);
       }
     } else if (warp == 1) {
@@ -571,7 +575,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         // ---- O += P · V, 8 MMAs of 128 x 256 x 16 per 64-token step ----
         const uint32_t idv = idesc_f16(128, 256, false, false, true);
         int ncmd = 0, nflush = 0, np = 0;
-        int64_t u = 0, tg = 0;
+        uint32_t u = 0, tg = 0;
         bool ok = true;
         const volatile int never = 0;
         Piece pc = first;
@@ -648,7 +652,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             break;
           }
           ++np;
-        } while (cur.next(p, pc));
+        } while (next_piece(pc));
         if (!ok) give_up(p, abort_flag, smem, peer);
         mma_commit(&bars[VB_FLUSH]);   // nothing may be in flight when the CTA leaves
         mbar_wait(&bars[VB_FLUSH], (uint32_t)(nflush & 1), &never, kWaitNs);
@@ -665,7 +669,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       griddep_wait();   // lse_part may still be read by the previous kernel of the stream
       mark_empty_sequences(p, pair, tid, 256);
       int k = 0, np = 0;
-      int64_t u_base = 0;   // first step of the current piece
+      uint32_t u_base = 0;   // first step of the current piece
       Piece pc = first;
       while (true) {
         if (!warp_wait(&bars[VB_CREQ], (uint32_t)(k & 1), abort_flag)) {
@@ -718,16 +722,21 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
         const float inv = good ? 1.f / l : 0.f;
         const int n_halves = 2 * piece_tiles(pc);
+        Piece nxt;
+        const bool more = next_piece(nxt);
         // Each row warp owns 32 heads x 256 columns: eight 32-column chunks, each scaled,
         // staged 128B-swizzled in a 4 KB buffer of the warp's own and written at once by a
-        // TMA store that the warp issues; two buffers per warp alternate, so the stores
-        // overlap the TMEM reads. The buffers lie in the stage of the piece's last step,
-        // which the producer refills only after VB_EPIFREE.
+        // TMA store that the warp issues; the buffers rotate, so the stores overlap the
+        // TMEM reads. Before another piece, two buffers per warp lie in the stage of the
+        // piece's last step, which the producer refills only after VB_EPIFREE; after the
+        // pair's last piece every stage is idle and each warp rotates six.
         const int rows = p.n_h < 128 ? p.n_h : 128;
         const int wrows = rows < 32 ? rows : 32;
         const bool wlive = 32 * q < rows;
-        unsigned char* wst = smem + V_CST + (int)((u_base + n_halves - 1) % kCStages) * kCStage +
-                             (warp - 2) * 2 * kEpiBuf;
+        const int nbuf = more ? 2 : 6;
+        unsigned char* wst = more ? smem + V_CST + (int)((u_base + n_halves - 1) % kCStages) * kCStage +
+                                        (warp - 2) * 2 * kEpiBuf
+                                  : smem + V_CST + (warp - 2) * 6 * kEpiBuf;
         const int64_t orow0 = part_row(p, pc.b, pc.slot) + 32 * q;
         uint32_t r[32];
 #pragma unroll 1
@@ -740,9 +749,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             mbar_arrive(&bars[VB_CDONE]);
           }
           if (!wlive) continue;
-          unsigned char* buf = wst + (cc & 1) * kEpiBuf;
-          if (cc >= 2) {   // this buffer's previous store has to have read it
-            if (lane == 0) bulk_wait_group_read<1>();
+          unsigned char* buf = wst + (cc % nbuf) * kEpiBuf;
+          if (cc >= nbuf) {   // this buffer's previous store has to have read it
+            if (lane == 0) {
+              if (more) bulk_wait_group_read<1>();
+              else bulk_wait_group_read<5>();
+            }
             __syncwarp();
           }
           if (lane < wrows) {
@@ -768,7 +780,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         if (pc.fill_from < p.S) fill_unused_slots(p, pc.b, pc.fill_from, tid, 256);
         u_base += n_halves;
         ++np;
-        if (!cur.next(p, pc)) pc.en = pc.st;   // no further epilogue follows
+        if (more) pc = nxt;
+        else pc.en = pc.st;   // no further epilogue follows
       }
       if (lane == 0) bulk_wait_group0();   // the partial results are written before the CTA may leave
       tc_fence_before();
@@ -845,13 +858,17 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const float scale_log2 = p.scale * 1.4426950408889634f;
-  const int64_t pairs = p.balanced ? (int64_t)p.pairs : (int64_t)p.B * p.S_used;
-  return launch_overlapped(decode_tc_kernel, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmemBytes, st, p, smap,
-                           vmap, qmap, omap, scale_log2);
+  if (p.balanced)
+    return launch_overlapped(decode_tc_kernel<true>, dim3((unsigned)(2 * p.pairs)), dim3(kThreads), kSmemBytes, st, p,
+                             smap, vmap, qmap, omap, scale_log2);
+  return launch_overlapped(decode_tc_kernel<false>, dim3((unsigned)(2 * (int64_t)p.B * p.S_used)), dim3(kThreads),
+                           kSmemBytes, st, p, smap, vmap, qmap, omap, scale_log2);
 }
 
 int decode_tc_num_splits(int B, int tiles, int n_h, int sms) {

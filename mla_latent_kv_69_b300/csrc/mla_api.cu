@@ -146,10 +146,14 @@ mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32
   p.balanced = 0;
   p.pairs = 0;
   if (num_splits == 0) {
-    if (cache->dtype == MLA_KV_BF16) {   // the persistent kernel shares the batch out evenly
+    if (cache->dtype == MLA_KV_BF16 && cache->block_table) {
+      // paged caches (ragged batches): the persistent kernel shares the batch's tiles out
+      // evenly over all SM pairs
       p.balanced = 1;
       p.pairs = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
-    } else {                             // uniform splits within the slots
+    } else {
+      // contiguous caches and e4m3: one pair per (sequence, split), uniform splits sized
+      // for the longest sequence, within the slots
       const int tiles = ceil_div(max_seq_len, kPage);
       const int su = tiles <= 1 ? 1 : decode_tc_num_splits(B, tiles, n_h, sm_count());
       p.S_used = su < S ? su : S;

@@ -1,9 +1,10 @@
 // Host-side check of the decode kernels' work schedule (the quota rule and the piece
 // cursor of decode_tc.cuh, compiled for the host). Reads cases from stdin, one per line:
 //     B S pairs L_0 ... L_{B-1}
-// and for each prints "ok <max tiles of a pair> <ceil(T / pairs)> <pieces>" or
-// "fail <reason>". Every pair's share is set up the way the kernel's sched_init does it
-// (prefix sums of the sequences' tile counts), then walked piece by piece.
+// and for each prints "ok <max tiles of a pair> <ceil(T / pairs)> <pieces> <split>" or
+// "fail <reason>" (split: the pieces per sequence of the split plan, 0 for the tile plan).
+// Every pair's share is set up the way the kernel's sched_init does it (tile counts,
+// their prefix sums and sched_plan), then walked piece by piece.
 #include <cstdio>
 #include <cstdlib>
 #include <string>
@@ -14,7 +15,7 @@
 using namespace mla;
 
 static std::string run_case(int B, int S, int pairs, const std::vector<int32_t>& lens, long long* max_tiles,
-                            long long* ideal, long long* npieces) {
+                            long long* ideal, long long* npieces, int* split) {
   DecodeParams p{};
   p.B = B;
   p.S = S;
@@ -32,20 +33,29 @@ static std::string run_case(int B, int S, int pairs, const std::vector<int32_t>&
     T += tiles[b];
     Tmax = std::max<int>(Tmax, (int)tiles[b]);
   }
-  const long long q = sched_quota(T, Tmax, S, pairs);
+  int Tmin = B > 0 ? (int)tiles[0] : 0;
+  for (int b = 0; b < B; ++b) Tmin = std::min<int>(Tmin, (int)tiles[b]);
   *ideal = (T + pairs - 1) / pairs;
   *max_tiles = 0;
   *npieces = 0;
   std::vector<std::vector<char>> covered(B);
   for (int b = 0; b < B; ++b) covered[b].assign(std::max(lens[b], 0), 0);
   std::vector<int> next_slot(B, 0), lasts(B, 0);
+  long long quota = 0;
   for (int pr = 0; pr < pairs; ++pr) {
     SchedShared sh{};
-    sh.q = q;
-    sh.t_begin = (long long)pr * q;
-    sh.t_end = std::min<long long>((long long)(pr + 1) * q, T);
+    int bn = 0;
+    int64_t bc = -1;
+    if (Tmin == Tmax && Tmax >= 1) sched_best_split(B, Tmax, S, pairs, &bn, &bc);
+    sched_plan(T, B, Tmin, Tmax, S, pairs, pr, bn, bc, &sh);
+    *split = sh.split;
+    if (sh.split > 0) {
+      quota = (((long long)B * sh.split + pairs - 1) / pairs) * sh.per;
+    } else {
+      quota = sh.q;
+    }
     sh.b0 = -1;
-    for (int b = 0; b < B && sh.t_begin < sh.t_end; ++b)
+    for (int b = 0; b < B && sh.split == 0 && sh.t_begin < sh.t_end; ++b)
       if (first[b] <= sh.t_begin && sh.t_begin < first[b] + tiles[b]) {
         sh.b0 = b;
         sh.c0 = first[b];
@@ -76,7 +86,7 @@ static std::string run_case(int B, int S, int pairs, const std::vector<int32_t>&
       mine += (pc.en - pc.st + kSchedTile - 1) / kSchedTile;
     }
     *max_tiles = std::max(*max_tiles, mine);
-    if (mine > q) return "pair above its quota";
+    if (mine > quota) return "pair above its quota";
   }
   for (int b = 0; b < B; ++b) {
     for (size_t t = 0; t < covered[b].size(); ++t)
@@ -93,9 +103,10 @@ int main() {
     for (int b = 0; b < B; ++b)
       if (std::scanf("%d", &lens[b]) != 1) return 2;
     long long mt = 0, ideal = 0, np = 0;
-    const std::string err = run_case(B, S, pairs, lens, &mt, &ideal, &np);
+    int split = 0;
+    const std::string err = run_case(B, S, pairs, lens, &mt, &ideal, &np, &split);
     if (err.empty())
-      std::printf("ok %lld %lld %lld\n", mt, ideal, np);
+      std::printf("ok %lld %lld %lld %d\n", mt, ideal, np, split);
     else
       std::printf("fail %s\n", err.c_str());
   }

@@ -298,3 +298,33 @@ def test_row_and_query_magnitudes(cuda_device, kv, paged):
     if kv == "fp8":
         for b in range(case.B):
             _fp8_codes_match(case, b)
+
+
+@pytest.mark.parametrize("name,lens", [
+    # ragged: about 480 tiles on the SM pairs, so pairs walk several pieces of several sequences
+    ("many_ragged", list(np.random.default_rng(61).integers(1, 700, size=160))),
+    # equal tile counts: each sequence cut into equal pieces (the split plan)
+    ("equal_lengths", [5120, 5100, 5080]),
+])
+def test_paged_persistent_schedule(cuda_device, name, lens):
+    """The paged cache under the library schedule runs the persistent kernel: every slot's
+    piece of every sequence, merged, against the latent form of the oracle (absorbed query
+    drawn directly), every head of every sequence."""
+    w = W.Workload("sched", n_h=128, batch=len(lens), ctx=0, paged=True, seed=62)
+    case = Case(w, cuda_device, lens=lens, keep_rows=True)
+    q_lat_bits = W.gen_q_lat(w)
+    q_lat = bits_to_torch_bf16(q_lat_bits, cuda_device)
+    q64 = rows_f32(q_lat_bits).astype(np.float64)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    o_part, lse_part = mla.decode_fwd(q_lat, case.cache, case.seq_lens, case.max_len, n_splits=0, status=status)
+    o_lat, lse = mla.combine(o_part, lse_part)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_lat, lse = o_lat.double().cpu().numpy(), lse.double().cpu().numpy()
+    got, ref = [], []
+    for b in range(case.B):
+        r = mla_oracle.attend_latent(q64[b], case.oracle_rows(b))
+        got.append(o_lat[b].ravel())
+        ref.append(r["o_lat"].ravel())
+        np.testing.assert_allclose(lse[b], r["lse"], rtol=2e-5, atol=2e-4)
+    assert_within_tolerance(np.concatenate(got), np.concatenate(ref), "o_lat")

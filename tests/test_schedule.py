@@ -2,7 +2,8 @@
 decode_tc.cuh, compiled for the CPU by tests/schedule_harness.cu, walked for every SM pair
 over many batch shapes. Every token is covered exactly once, every sequence's pieces take
 slots 0, 1, ... in token order below the slot count the library reports
-(mla_num_splits), the last piece marks the unused slots, and no pair exceeds its quota."""
+(mla_num_splits), the last piece marks the unused slots, and no pair exceeds its quota.
+Batches of equal lengths take the split plan when it spares pairs a second piece."""
 
 import os
 import shutil
@@ -53,12 +54,26 @@ def test_workload_schedules_are_exact_and_balanced(harness):
         w = W.WORKLOADS[name]
         lens = W.seq_lens(w)
         cases.append((w.batch, _slots(w.batch, lens), PAIRS, lens))
-    for (B, S, P, lens), res in zip(cases, _run(harness, cases)):
+    plans = {}
+    for name, (B, S, P, lens), res in zip(W.WORKLOAD_ORDER, cases, _run(harness, cases)):
         assert res[0] == "ok", (B, res)
-        max_tiles, ideal = int(res[1]), int(res[2])
+        max_tiles, ideal, split = int(res[1]), int(res[2]), int(res[4])
         T = int(np.sum((lens + 127) // 128))
-        # the slot count leaves the quota at the even share for these shapes
-        assert max_tiles == ideal == -(-T // P), (B, max_tiles, ideal)
+        assert ideal == -(-T // P)
+        if split == 0:
+            # the slot count leaves the quota at the even share for these shapes
+            assert max_tiles == ideal, (B, max_tiles, ideal)
+        else:
+            tiles = (lens + 127) // 128
+            assert np.all(tiles == tiles[0])
+            per = -(-int(tiles[0]) // split)
+            assert max_tiles == -(-B * split // P) * per
+            assert max_tiles <= ideal + 3   # cheaper than the tile plan's piece switch
+        plans[name] = (split, max_tiles)
+    # equal lengths are cut into whole pieces (no pair holds two), ragged batches share tiles
+    assert plans["v2_b32_l4096"] == (2, 16)
+    assert plans["long_b4_l128k"] == (18, 57)
+    assert plans["paged_b64_l1k_32k"][0] == 0
 
 
 def test_random_batches(harness):
@@ -81,6 +96,9 @@ def test_random_batches(harness):
         cases.append((B, S, P, lens.astype(np.int64)))
     for case, res in zip(cases, _run(harness, cases)):
         assert res[0] == "ok", (case[0], case[1], case[2], " ".join(res))
+        tiles = (case[3] + 127) // 128
+        if int(res[4]) > 0:   # the split plan only for equal, nonzero tile counts, within the slots
+            assert np.all(tiles == tiles[0]) and tiles[0] > 0 and int(res[4]) <= case[1]
 
 
 def test_slot_count_rule():
