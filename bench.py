@@ -381,11 +381,11 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=0, bufs=e2e_bufs)
         h_o.copy_(e2e_bufs["o"], non_blocking=True)
 
-    for _ in range(max(args.warmup, 1)):
+    for _ in range(max(args.warmup, 10)):   # first calls pay one-time host setup
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms, host_ms = [], []
-    for _ in range(K):
+    for _ in range(max(K, 30)):
         flush_l2()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -450,6 +450,9 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         "cache_gbs_decode_combine": round(cache_bytes / ((decode_ms + float(kern_ms[2])) / 1e3) / 1e9, 1),
         "e2e": {"value": round(total_cache / (e2e_mean / 1e3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_mean, 5), "host_ms_per_step": round(float(np.mean(host_ms)), 4),
+                "steps": len(e2e_ms), "ms_median": round(float(np.median(e2e_ms)), 5),
+                "ms_max": round(float(np.max(e2e_ms)), 5),
+                "device_step_ratio": round(e2e_mean / step_ms, 2),
                 "h2d_bytes_per_step": int(h_q.numel() * 2 + h_pos.numel() * 4 + h_len.numel() * 4),
                 "d2h_bytes_per_step": int(h_o.numel() * 4),
                 "path": "mla.decode_step (the public Python call over the C ABI) with pinned host buffers"},

@@ -45,8 +45,13 @@ def default_scale() -> float:
     return 1.0 / math.sqrt(D_NOPE + D_ROPE)
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device=None) -> int:
     if stream is None:
+        if _raw_stream is not None and device is not None and device.index is not None:
+            return int(_raw_stream(device.index))   # the device's current torch stream, as a handle
         stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -72,8 +77,12 @@ def _one_device(**tensors):
 def _call(fn: str, device, *args, stream=None):
     """Run one C-ABI call with `device` current, on `stream` (default: that device's
     current torch stream), and raise MlaError on a non-OK status."""
+    f = getattr(_lib.get(), fn)
+    if device.index is not None and device.index == torch.cuda.current_device():
+        check(fn, f(*args, _stream(stream, device)))
+        return
     with torch.cuda.device(device):
-        check(fn, getattr(_lib.get(), fn)(*args, _stream(stream, device)))
+        check(fn, f(*args, _stream(stream, device)))
 
 
 def _ptr(t) -> int | None:
@@ -120,6 +129,18 @@ class Cache:
         return MLA_KV_FP8_E4M3 if self.data.dtype in (torch.uint8, torch.float8_e4m3fn) else MLA_KV_BF16
 
     def to_c(self) -> MlaCache:
+        """The C view of the cache, built and checked once per set of tensors (a serving
+        loop passes the same cache every step)."""
+        key = tuple((id(t), t.data_ptr(), tuple(t.shape), t.dtype) if t is not None else None
+                    for t in (self.data, self.scales, self.block_table))
+        memo = self.__dict__.get("_c_memo")
+        if memo is not None and memo[0] == key:
+            return memo[1]
+        c = self._build_c()
+        self.__dict__["_c_memo"] = (key, c)
+        return c
+
+    def _build_c(self) -> MlaCache:
         d = self.data
         if d.dtype not in (torch.bfloat16, torch.uint8, torch.float8_e4m3fn):
             raise TypeError("cache data must be bf16 or uint8/float8_e4m3fn codes")

@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -180,58 +181,51 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
   if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult qr;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
+// Fixed-point turns per position of the 32 RoPE frequencies of `base` (2^64 units of a
+// full turn), computed once per base.
+RopeTurns rope_turns(float rope_base) {
+  static std::mutex mu;
+  static float last_base = 0.f;
+  static RopeTurns last;
+  std::lock_guard<std::mutex> lock(mu);
+  if (rope_base != last_base) {
+    for (int i = 0; i < kRope / 2; ++i) {
+      const double f = std::pow((double)rope_base, -2.0 * i / (double)kRope) / (2.0 * M_PI);   // < 1/(2 pi)
+      last.f[i] = (unsigned long long)std::ldexp(f, 64);
+    }
+    last_base = rope_base;
+  }
+  return last;
 }
 
 }  // namespace
 
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const int32_t* pos,
                             int B, int n_h, float rope_base, __nv_bfloat16* q_lat, cudaStream_t st) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorInvalidValue;
   // W_UK viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = one M-tile (2 chunks)
   CUtensorMap wmap, qmap;
   {
-    cuuint64_t dims[3] = {64, (cuuint64_t)n_h * kNope, kLatent / 64};
-    cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, 128};
-    cuuint32_t box[3] = {64, kNope, 2};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (fn(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(w_uk), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const uint64_t dims[3] = {64, (uint64_t)n_h * kNope, kLatent / 64};
+    const uint64_t strides[2] = {(uint64_t)kLatent * 2, 128};
+    const uint32_t box[3] = {64, kNope, 2};
+    if (!encode_tiled(tmap_desc(w_uk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      &wmap))
       return cudaErrorInvalidValue;
   }
   // q viewed as (64 d, head, sequence, 64-d chunk); box = one head, 128 sequences, q^C's 2 chunks
   {
-    cuuint64_t dims[4] = {64, (cuuint64_t)n_h, (cuuint64_t)B, 3};
-    cuuint64_t strides[3] = {(cuuint64_t)kQ * 2, (cuuint64_t)n_h * kQ * 2, 128};
-    cuuint32_t box[4] = {64, 1, kNB, 2};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<__nv_bfloat16*>(q), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const uint64_t dims[4] = {64, (uint64_t)n_h, (uint64_t)B, 3};
+    const uint64_t strides[3] = {(uint64_t)kQ * 2, (uint64_t)n_h * kQ * 2, 128};
+    const uint32_t box[4] = {64, 1, kNB, 2};
+    if (!encode_tiled(tmap_desc(q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      &qmap))
       return cudaErrorInvalidValue;
   }
-  RopeTurns turns;
-  for (int i = 0; i < kRope / 2; ++i) {
-    const double f = std::pow((double)rope_base, -2.0 * i / (double)kRope) / (2.0 * M_PI);   // < 1/(2 pi)
-    turns.f[i] = (unsigned long long)std::ldexp(f, 64);
-  }
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(absorb_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  });
+  const RopeTurns turns = rope_turns(rope_base);
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t attr_err = smem_attr_once(absorb_q_tc, kSmem, attr_done);
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(n_h, ceil_div(B, kNB));
   return launch_overlapped(absorb_q_tc, grid, dim3(kThreads), kSmem, st, wmap, qmap, q, pos, B, n_h, turns, q_lat);

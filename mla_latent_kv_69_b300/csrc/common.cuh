@@ -1,6 +1,7 @@
 // Shared device/host helpers for the MLA decode library (sm_103a).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
@@ -18,6 +19,7 @@ constexpr int kLatent = MLA_D_LATENT;  // 512
 constexpr int kRow = MLA_D_ROW;        // 576
 constexpr int kQ = MLA_D_Q;            // 192
 constexpr int kPage = MLA_PAGE_SIZE;   // 64
+constexpr int kMaxDevices = 64;
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -100,6 +102,21 @@ namespace mla {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// device (the attribute belongs to the device's copy of the kernel). `done` is the call
+// site's own flag table.
+template <typename... KArgs>
+cudaError_t smem_attr_once(void (*kernel)(KArgs...), int bytes, std::atomic<int> (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+  return e;
 }
 
 // Launch `kernel` so that it may overlap the tail of the previous kernel on `st`.

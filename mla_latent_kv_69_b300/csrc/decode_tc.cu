@@ -49,6 +49,7 @@
 
 #include "decode_tc.cuh"
 #include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -795,46 +796,27 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
 }
 
 // ------------------------------------ host side ---------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 // 3D map over rows of 576 bf16 seen as (64 columns, row, 64-column chunk), the chunk
 // stride being 128 bytes; a box of `box_rows` rows x `box_chunks` chunks lands in
 // shared memory chunk-major, each chunk a 128B-swizzled [box_rows][64] block.
 bool make_row_map(const void* base, int64_t rows, int box_rows, int box_chunks, CUtensorMap* map) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
-  cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {64, (uint64_t)rows, (uint64_t)(kRow / 64)};
+  const uint64_t strides[2] = {(uint64_t)kRow * 2, 128};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, (uint32_t)box_chunks};
+  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      map);
 }
 
 // 3D map over the fp32 partial results [rows][512] seen as (32 values, row, 16 chunks of
 // 32), 128B swizzle; a box is `box_rows` rows (32, or n_h when smaller) x one chunk.
 bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)(kLatent / 32)};
-  cuuint64_t strides[2] = {(cuuint64_t)kLatent * 4, 128};
-  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  const uint64_t dims[3] = {32, (uint64_t)rows, (uint64_t)(kLatent / 32)};
+  const uint64_t strides[2] = {(uint64_t)kLatent * 4, 128};
+  const uint32_t box[3] = {32, (uint32_t)box_rows, 1};
+  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE),
+                      map);
 }
 
 }  // namespace
@@ -855,13 +837,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
       !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap) ||
       !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 32 ? p.n_h : 32, &omap))
     return cudaErrorInvalidValue;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
+  static std::atomic<int> attr_multi[kMaxDevices], attr_single[kMaxDevices];
+  const cudaError_t attr_err = p.balanced ? smem_attr_once(decode_tc_kernel<true>, kSmemBytes, attr_multi)
+                                          : smem_attr_once(decode_tc_kernel<false>, kSmemBytes, attr_single);
   if (attr_err != cudaSuccess) return attr_err;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   if (p.balanced)

@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "decode_tc.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -776,57 +777,35 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
   cluster_sync();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult qr;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 // 3D map over rows of 576 e4m3 codes seen as (64 codes, row, 9 chunks of 64 codes),
 // no swizzle; a box of `box_rows` rows x `box_chunks` chunks lands chunk-major.
 bool make_code_map(const void* base, int64_t rows, int box_rows, int box_chunks, CUtensorMap* map) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
-  cuuint64_t strides[2] = {(cuuint64_t)kRow, 64};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {64, (uint64_t)rows, (uint64_t)(kRow / 64)};
+  const uint64_t strides[2] = {(uint64_t)kRow, 64};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, (uint32_t)box_chunks};
+  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      map);
 }
 
 bool make_q_map(const void* base, int64_t rows, int box_rows, CUtensorMap* map) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
-  cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 3};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {64, (uint64_t)rows, (uint64_t)(kRow / 64)};
+  const uint64_t strides[2] = {(uint64_t)kRow * 2, 128};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, 3};
+  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      map);
 }
 
 // fp32 partial results [rows][512] as (32 values, row, 16 chunks of 32), 128B swizzle;
 // a box is `box_rows` rows x one chunk (one row warp's store).
 bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)(kLatent / 32)};
-  cuuint64_t strides[2] = {(cuuint64_t)kLatent * 4, 128};
-  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  const uint64_t dims[3] = {32, (uint64_t)rows, (uint64_t)(kLatent / 32)};
+  const uint64_t strides[2] = {(uint64_t)kLatent * 4, 128};
+  const uint32_t box[3] = {32, (uint32_t)box_rows, 1};
+  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE),
+                      map);
 }
 
 }  // namespace
@@ -838,11 +817,8 @@ cudaError_t launch_decode_tc_fp8(const DecodeParams& p, cudaStream_t st) {
       !make_q_map(p.q_lat, (int64_t)p.B * p.n_h, rows, &qmap) ||
       !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 32 ? p.n_h : 32, &omap))
     return cudaErrorInvalidValue;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(decode_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t attr_err = smem_attr_once(decode_tc_fp8_kernel, kSmemBytes, attr_done);
   if (attr_err != cudaSuccess) return attr_err;
   // 2^8: the f16 operands hold 2^-8 times the codes' values
   const float scale_log2 = p.scale * 1.4426950408889634f * 256.f;

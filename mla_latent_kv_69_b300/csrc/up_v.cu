@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -173,40 +174,21 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
   if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 64);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult qr;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 }  // namespace
 
 cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, int n_h, float* o,
                         cudaStream_t st) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorInvalidValue;
   // W_UV viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = 128 d rows x two chunks
   CUtensorMap wmap;
-  cuuint64_t dims[3] = {64, (cuuint64_t)n_h * kNope, kChunks};
-  cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, 128};
-  cuuint32_t box[3] = {64, kNope, 2};
-  cuuint32_t es[3] = {1, 1, 1};
-  if (fn(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(w_uv), dims, strides, box, es,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const uint64_t dims[3] = {64, (uint64_t)n_h * kNope, kChunks};
+  const uint64_t strides[2] = {(uint64_t)kLatent * 2, 128};
+  const uint32_t box[3] = {64, kNope, 2};
+  if (!encode_tiled(tmap_desc(w_uv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                    &wmap))
     return cudaErrorInvalidValue;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(up_v_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  });
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t attr_err = smem_attr_once(up_v_tc, kSmem, attr_done);
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(n_h, ceil_div(B, kNB));
   return launch_overlapped(up_v_tc, grid, dim3(kThreads), kSmem, st, wmap, o_lat, B, n_h, o);
