@@ -366,7 +366,9 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     step_ms_max = dist.max(step_ms, dev)
 
     # e2e through the public API with host buffers: per step, H2D of the new queries
-    # (+ positions, lengths) from pinned memory, the four calls, and D2H of o.
+    # (+ positions, lengths) from pinned memory, the four calls, and D2H of o. The
+    # headline form replays the step captured once as a CUDA graph (mla.DecodeStepGraph);
+    # the eager form makes the four Python calls every step (mla.decode_step).
     h_q = case.q.cpu().pin_memory()
     h_pos = case.pos.cpu().pin_memory()
     h_len = case.seq_lens.cpu().pin_memory()
@@ -374,29 +376,43 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     d_q, d_pos, d_len = torch.empty_like(case.q), torch.empty_like(case.pos), torch.empty_like(case.seq_lens)
     e2e_bufs = dict(bufs)
 
-    def e2e_step():
+    def eager_step():
         d_q.copy_(h_q, non_blocking=True)
         d_pos.copy_(h_pos, non_blocking=True)
         d_len.copy_(h_len, non_blocking=True)
         mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=0, bufs=e2e_bufs)
         h_o.copy_(e2e_bufs["o"], non_blocking=True)
 
-    for _ in range(max(args.warmup, 10)):   # first calls pay one-time host setup
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms, host_ms = [], []
-    for _ in range(max(K, 30)):
-        flush_l2()
+    g = mla.DecodeStepGraph(case.w_uk, case.w_uv, cache, B, case.max_len)
+    g.h_q.copy_(h_q)
+    g.h_pos.copy_(h_pos)
+    g.h_seq_lens.copy_(h_len)
+
+    def time_e2e(run, st):
+        for _ in range(max(args.warmup, 10)):   # first calls pay one-time host setup
+            run()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        t0 = time.perf_counter()
-        e2e_step()
-        host_ms.append(1e3 * (time.perf_counter() - t0))
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
+        e2e_ms, host_ms = [], []
+        for _ in range(max(K, 30)):
+            flush_l2()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            t0 = time.perf_counter()
+            run()
+            host_ms.append(1e3 * (time.perf_counter() - t0))
+            b.record(st)
+            b.synchronize()
+            e2e_ms.append(a.elapsed_time(b))
+        return e2e_ms, host_ms
+
+    e2e_ms, host_ms = time_e2e(g.replay, g.stream)
+    eager_ms, eager_host_ms = time_e2e(eager_step, stream)
+    torch.cuda.synchronize()
+    same_o = bool(torch.equal(g.h_o, h_o))   # both forms computed the same step
     e2e_mean = dist.max(float(np.mean(e2e_ms)), dev)
+    eager_mean = dist.max(float(np.mean(eager_ms)), dev)
+    del g
 
     peaks, peaks_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -455,7 +471,15 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
                 "device_step_ratio": round(e2e_mean / step_ms, 2),
                 "h2d_bytes_per_step": int(h_q.numel() * 2 + h_pos.numel() * 4 + h_len.numel() * 4),
                 "d2h_bytes_per_step": int(h_o.numel() * 4),
-                "path": "mla.decode_step (the public Python call over the C ABI) with pinned host buffers"},
+                "path": "mla.DecodeStepGraph.replay (the step captured once over the C ABI: H2D of q, pos and "
+                        "seq_lens from pinned host buffers, the four calls, D2H of o)",
+                "same_o_as_eager": same_o,
+                "eager": {"value": round(total_cache / (eager_mean / 1e3) / 1e9, 2), "unit": "GB/s",
+                          "ms_per_step": round(eager_mean, 5),
+                          "host_ms_per_step": round(float(np.mean(eager_host_ms)), 4),
+                          "ms_median": round(float(np.median(eager_ms)), 5),
+                          "path": "mla.decode_step (four Python calls over the C ABI each step) with the same "
+                                  "pinned host buffers and copies"}},
         "clocks": {**clocks, "window": f"{args.soak:.1f} s soak + the timed steps"},
     }
     del case, cache, bufs, e2e_bufs, flush, drain, graph, graph_parts

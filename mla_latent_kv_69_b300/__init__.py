@@ -30,7 +30,8 @@ __all__ = [
     "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range", "decode_kernel",
     "decode_combine_static",
     "compute_dtype",
-    "Cache", "MlaError", "status_string", "default_scale", "decode_step", "lib_path", "MLA_MAX_SPLITS",
+    "Cache", "MlaError", "status_string", "default_scale", "decode_step", "DecodeStepGraph", "lib_path",
+    "MLA_MAX_SPLITS", "test_decode_stalled",
 ]
 
 D_NOPE, D_ROPE, D_LATENT, D_ROW, D_Q, PAGE = 128, 64, 512, 576, 192, 64
@@ -229,6 +230,32 @@ def decode_fwd(q_lat, cache: Cache, seq_lens, max_seq_len: int, softmax_scale: f
     return o_part, lse_part
 
 
+def test_decode_stalled(q_lat, cache: Cache, seq_lens, max_seq_len: int, status, wait_ns: int,
+                        n_splits: int = 0, o_part=None, lse_part=None, stream=None):
+    """Test hook (include/mla_test.h): decode_fwd with the cache loads withheld and the
+    given wait limit, so the kernel's bounded waits run out and it records
+    MLA_ERR_TIMEOUT in `status`. Not part of a decode step."""
+    B, n_h = q_lat.shape[0], q_lat.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, (B, n_h, D_ROW))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _need(status, "status", torch.int32)
+    S = n_splits if n_splits > 0 else num_splits(B, max_seq_len, n_h)
+    if o_part is None:
+        o_part = torch.empty(B, S, n_h, D_LATENT, dtype=torch.float32, device=q_lat.device)
+    if lse_part is None:
+        lse_part = torch.empty(B, S, n_h, dtype=torch.float32, device=q_lat.device)
+    _need(o_part, "o_part", torch.float32, (B, S, n_h, D_LATENT))
+    _need(lse_part, "lse_part", torch.float32, (B, S, n_h))
+    _need_table_rows(cache, B)
+    c = cache.to_c()
+    dev = _one_device(q_lat=q_lat, seq_lens=seq_lens, o_part=o_part, lse_part=lse_part, status=status,
+                      **cache.tensors())
+    _call("mla_test_decode_stalled", dev, _ptr(q_lat), ctypes.byref(c), _ptr(seq_lens), B, n_h, int(max_seq_len),
+          default_scale(), int(n_splits) if n_splits > 0 else 0, _ptr(o_part), _ptr(lse_part), _ptr(status),
+          int(wait_ns), stream=stream)
+    return o_part, lse_part
+
+
 def combine(o_part, lse_part, o_lat=None, lse=None, stream=None):
     B, S, n_h = o_part.shape[0], o_part.shape[1], o_part.shape[2]
     _need(o_part, "o_part", torch.float32, (B, S, n_h, D_LATENT))
@@ -307,3 +334,71 @@ def decode_step(q, w_uk, w_uv, cache: Cache, seq_lens, pos, max_seq_len: int, n_
     o_lat, lse = combine(o_part, lse_part, o_lat=bufs.get("o_lat"), lse=bufs.get("lse"), stream=stream)
     o = up_v(o_lat, w_uv, o=bufs.get("o"), stream=stream)
     return dict(q_lat=q_lat, o_part=o_part, lse_part=lse_part, o_lat=o_lat, lse=lse, o=o)
+
+
+class DecodeStepGraph:
+    """One decode step of one layer, captured once as a CUDA graph and replayed per step.
+
+    A serving loop repeats the same step on the same buffers, so the host work of the
+    four calls (argument checks, tensor maps, launches) is paid once, at capture. The
+    graph holds, in order: the copy of the step's inputs from pinned host buffers
+    (`h_q`, `h_pos`, `h_seq_lens`, which the caller fills before each step), the four
+    C-ABI calls, and the copy of `o` into the pinned host buffer `h_o`.
+
+        g = DecodeStepGraph(w_uk, w_uv, cache, B, max_seq_len)
+        g.h_q.copy_(...); g.h_pos.copy_(...); g.h_seq_lens.copy_(...)
+        g.replay(); g.synchronize()          # g.h_o holds o [B, n_h, 128] fp32
+
+    The cache tensors and weights are captured by address: they must stay allocated
+    (their contents may change between steps, e.g. appended tokens). max_seq_len bounds
+    every later seq_lens, as for decode_fwd.
+    """
+
+    def __init__(self, w_uk, w_uv, cache: Cache, B: int, max_seq_len: int, n_splits: int = 0,
+                 softmax_scale: float | None = None, rope_base: float = 10000.0, status=None):
+        n_h = w_uk.shape[0]
+        dev = w_uk.device
+        self.device, self.B, self.n_h = dev, B, n_h
+        self.h_q = torch.empty(B, n_h, D_Q, dtype=torch.bfloat16).pin_memory()
+        self.h_pos = torch.zeros(B, dtype=torch.int32).pin_memory()
+        self.h_seq_lens = torch.zeros(B, dtype=torch.int32).pin_memory()
+        self.h_o = torch.empty(B, n_h, D_NOPE, dtype=torch.float32).pin_memory()
+        self.d_q = torch.zeros(B, n_h, D_Q, dtype=torch.bfloat16, device=dev)
+        self.d_pos = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.d_seq_lens = torch.zeros(B, dtype=torch.int32, device=dev)
+        S = n_splits if n_splits > 0 else num_splits(B, max_seq_len, n_h)
+        self.bufs = dict(
+            q_lat=torch.empty(B, n_h, D_ROW, dtype=torch.bfloat16, device=dev),
+            o_part=torch.empty(B, S, n_h, D_LATENT, dtype=torch.float32, device=dev),
+            lse_part=torch.empty(B, S, n_h, dtype=torch.float32, device=dev),
+            o_lat=torch.empty(B, n_h, D_LATENT, dtype=torch.float32, device=dev),
+            lse=torch.empty(B, n_h, dtype=torch.float32, device=dev),
+            o=torch.empty(B, n_h, D_NOPE, dtype=torch.float32, device=dev))
+        self.stream = torch.cuda.Stream(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        args = (w_uk, w_uv, cache, self.d_seq_lens, self.d_pos, max_seq_len)
+        kw = dict(n_splits=n_splits, softmax_scale=softmax_scale, rope_base=rope_base, bufs=self.bufs, status=status)
+        with torch.cuda.device(dev), torch.cuda.stream(self.stream):
+            # one eager step first: every argument check and launch path runs once outside capture
+            decode_step(self.d_q, *args, **kw)
+            self.stream.synchronize()
+            with torch.cuda.graph(self.graph, stream=self.stream):
+                self.d_q.copy_(self.h_q, non_blocking=True)
+                self.d_pos.copy_(self.h_pos, non_blocking=True)
+                self.d_seq_lens.copy_(self.h_seq_lens, non_blocking=True)
+                decode_step(self.d_q, *args, **kw)
+                self.h_o.copy_(self.bufs["o"], non_blocking=True)
+        self.done = torch.cuda.Event()
+
+    def replay(self):
+        """Queue one step on the graph's own stream, after the work already queued on the
+        caller's current stream (returns at once)."""
+        with torch.cuda.device(self.device):
+            self.stream.wait_stream(torch.cuda.current_stream(self.device))
+            with torch.cuda.stream(self.stream):
+                self.graph.replay()
+            self.done.record(self.stream)
+
+    def synchronize(self):
+        """Wait until the last replayed step's o is in h_o."""
+        self.done.synchronize()

@@ -61,6 +61,8 @@ struct DecodeParams {
   int32_t balanced;             // 1: balanced schedule over `pairs` SM pairs; 0: one pair per (b, split)
   int32_t pairs;                // balanced schedule: SM pairs sharing the batch
   float scale;                  // softmax scale (natural-log units)
+  uint64_t wait_ns;             // limit of the waits that an abort can end (0: the default, 2 s)
+  int32_t stall_loads;          // test hook: the score CTA issues no loads, so its consumers' waits run out
 };
 
 // Row index of token t (>= 0) of sequence b, or -1 when the token falls outside the

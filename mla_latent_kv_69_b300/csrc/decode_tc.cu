@@ -155,6 +155,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
   const uint32_t peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = blockIdx.x >> 1;
+  // waits an abort can end: the caller's limit (a test runs them out quickly); the drains
+  // of copies and tensor-core work already in flight keep the long limit
+  const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
   griddep_launch_dependents();
 
   if (smem_u32(smem) & 1023u) {   // the 128B swizzle needs 1024-byte aligned slots (same in both CTAs)
@@ -247,14 +250,16 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         prefetch_tmap(&qmap);
         griddep_wait();   // q_lat comes from the previous kernel
         uint32_t k = 0;
+        // test hook: no loads at all, so that every wait on them runs out
+        const bool issue = !p.stall_loads;
         bool ok = true;
         Piece pc = first;
         auto slot_ready = [&](uint32_t item) -> bool {   // the slot's previous item was consumed
           if (item < kRing) return true;
           return mbar_wait(&bars[SB_SLOT_EMPTY + (int)(item % kRing)], (uint32_t)(((item / kRing) - 1) & 1), abort_flag,
-                           kWaitNs);
+                           wait_ns);
         };
-        do {
+        while (issue) {
           const int n_tiles = piece_tiles(pc);
           for (int g = 0; g < 3 && ok; ++g, ++k) {
             if (!(ok = slot_ready(k))) break;
@@ -300,7 +305,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
               }
             }
           }
-        } while (ok && !*abort_flag && next_piece(pc));
+          if (!(ok && !*abort_flag && next_piece(pc))) break;
+        }
         if (!ok) give_up(p, abort_flag, smem, peer);
         // Loads still in flight land before the CTA may leave.
         const volatile int never = 0;
@@ -318,20 +324,20 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         do {
           const int n_tiles = piece_tiles(pc);
           k += 3;   // the query items (consumed by the softmax warps)
-          if (!mbar_wait(&bars[SB_QREADY], (uint32_t)(np & 1), abort_flag, kWaitNs)) {
+          if (!mbar_wait(&bars[SB_QREADY], (uint32_t)(np & 1), abort_flag, wait_ns)) {
             ok = false;
             break;
           }
           if (np == 0) mbar_arrive_remote(&bars[VB_GO], 1);   // the value CTA may start its loads
           for (int i = 0; ok && i < n_tiles; ++i, ++tg) {
-            if (tg > 0 && !mbar_wait(&bars[SB_SFREE], (uint32_t)((tg - 1) & 1), abort_flag, kWaitNs)) {
+            if (tg > 0 && !mbar_wait(&bars[SB_SFREE], (uint32_t)((tg - 1) & 1), abort_flag, wait_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
             for (int g = 0; g < 3; ++g, ++k) {
               const int r = (int)(k % kRing);
-              if (!mbar_wait(&bars[SB_SLOT_FULL + r], (uint32_t)((k / kRing) & 1), abort_flag, kWaitNs)) {
+              if (!mbar_wait(&bars[SB_SLOT_FULL + r], (uint32_t)((k / kRing) & 1), abort_flag, wait_ns)) {
                 ok = false;
                 break;
               }
@@ -378,7 +384,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         bool qok = true;
         for (int g = 0; g < 3; ++g)
           qok = qok && warp_wait(&bars[SB_SLOT_FULL + (int)((k + g) % kRing)], (uint32_t)(((k + g) / kRing) & 1),
-                                 abort_flag);
+                                 abort_flag, wait_ns);
         if (qok) {
 #pragma unroll 1
           for (int c = j; c < 9; c += 2) {
@@ -408,7 +414,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         int pg = page_ahead(p, pc.b, pc.st, j);   // this thread's half of the next tile, fetched ahead
         for (int i = 0; i < n_tiles; ++i, ++tg) {
           uint32_t sr[64];
-          const bool got = warp_wait(&bars[SB_SFULL], (uint32_t)(tg & 1), abort_flag);
+          const bool got = warp_wait(&bars[SB_SFULL], (uint32_t)(tg & 1), abort_flag, wait_ns);
           if (got) {
             tc_fence_after();
             MLA_TMEM_LD32(trow + kSCol + 64 * j, sr);
@@ -478,7 +484,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
           }
           l_run += lsum;
           // The staging panel is free once the value CTA's PV on the previous tile has read it.
-          if (tg > 0) mbar_wait<true>(&bars[SB_PFREE + j], (uint32_t)((tg - 1) & 1), abort_flag, kWaitNs);
+          if (tg > 0) mbar_wait<true>(&bars[SB_PFREE + j], (uint32_t)((tg - 1) & 1), abort_flag, wait_ns);
           unsigned char* stg = smem + S_PANEL + j * kPanel;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
@@ -529,11 +535,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         int epi_done = 0;      // epilogues confirmed
         auto wait_epi = [&](int n) -> bool {
           for (; epi_done <= n; ++epi_done)
-            if (!mbar_wait(&bars[VB_EPIFREE], (uint32_t)(epi_done & 1), abort_flag, kWaitNs)) return false;
+            if (!mbar_wait(&bars[VB_EPIFREE], (uint32_t)(epi_done & 1), abort_flag, wait_ns)) return false;
           return true;
         };
         // Start once the score CTA has its first query: its query load goes first.
-        if (!mbar_wait<true>(&bars[VB_GO], 0, abort_flag, kWaitNs)) ok = false;
+        if (!mbar_wait<true>(&bars[VB_GO], 0, abort_flag, wait_ns)) ok = false;
         Piece pc = first;
         while (ok && !*abort_flag) {
           const int n_halves = 2 * piece_tiles(pc);
@@ -544,7 +550,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
           for (int ul = 0; ok && ul < n_halves && !*abort_flag; ++ul, ++u) {
             const int sg = (int)(u % kCStages);
             if (u >= kCStages &&
-                !mbar_wait(&bars[VB_CEMPTY + sg], (uint32_t)(((u / kCStages) - 1) & 1), abort_flag, kWaitNs)) {
+                !mbar_wait(&bars[VB_CEMPTY + sg], (uint32_t)(((u / kCStages) - 1) & 1), abort_flag, wait_ns)) {
               ok = false;
               break;
             }
@@ -583,7 +589,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         auto command = [&](int c) -> bool {   // hand a command to the row warps and wait for it
           *cmd_word = c;
           mbar_arrive(&bars[VB_CREQ]);
-          const bool done = mbar_wait(&bars[VB_CDONE], (uint32_t)(ncmd & 1), abort_flag, kWaitNs);
+          const bool done = mbar_wait(&bars[VB_CDONE], (uint32_t)(ncmd & 1), abort_flag, wait_ns);
           ++ncmd;
           return done;
         };
@@ -593,8 +599,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
           int pg = page_ahead(p, pc.b, pc.st, 0);
           for (int ul = 0; ul < n_halves; ++ul, ++u) {
             const int j = ul & 1, sg = (int)(u % kCStages);
-            if (!mbar_wait(&bars[VB_CFULL + sg], (uint32_t)((u / kCStages) & 1), abort_flag, kWaitNs) ||
-                !mbar_wait<true>(&bars[VB_PFULL + j], (uint32_t)(tg & 1), abort_flag, kWaitNs)) {
+            if (!mbar_wait(&bars[VB_CFULL + sg], (uint32_t)((u / kCStages) & 1), abort_flag, wait_ns) ||
+                !mbar_wait<true>(&bars[VB_PFULL + j], (uint32_t)(tg & 1), abort_flag, wait_ns)) {
               ok = false;
               break;
             }
@@ -673,7 +679,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
       uint32_t u_base = 0;   // first step of the current piece
       Piece pc = first;
       while (true) {
-        if (!warp_wait(&bars[VB_CREQ], (uint32_t)(k & 1), abort_flag)) {
+        if (!warp_wait(&bars[VB_CREQ], (uint32_t)(k & 1), abort_flag, wait_ns)) {
           give_up(p, abort_flag, smem, peer);
           break;
         }
@@ -715,7 +721,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         // ---- epilogue of piece np: o_part = O / l, lse_part = (m + log2 l) · ln 2 ----
         griddep_wait();   // o_part may still be read by the previous kernel of the stream
         const int f = np & 1;
-        const bool fin_ok = warp_wait<true>(&bars[VB_FIN + f], (uint32_t)((np >> 1) & 1), abort_flag);
+        const bool fin_ok = warp_wait<true>(&bars[VB_FIN + f], (uint32_t)((np >> 1) & 1), abort_flag, wait_ns);
         tc_fence_after();
         const float* fin = reinterpret_cast<const float*>(smem + V_FIN + f * kFin);
         const float m = fin[2 * h];

@@ -64,8 +64,9 @@ __device__ __forceinline__ HalfInfo half_info(const DecodeParams& p, int b, int 
 // A bounded wait taken by all 32 lanes of a warp together: every lane returns the same
 // answer, so warp-collective code after it never runs with lanes missing.
 template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
-  const bool ok = sm100::mbar_wait<kCluster>(bar, parity, abort_flag, kDecodeWaitNs);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint64_t limit_ns = kDecodeWaitNs) {
+  const bool ok = sm100::mbar_wait<kCluster>(bar, parity, abort_flag, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

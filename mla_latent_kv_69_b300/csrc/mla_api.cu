@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "decode_tc.cuh"
+#include "mla_test.h"
 
 namespace {
 
@@ -93,9 +94,14 @@ mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* pos, int
                                      static_cast<__nv_bfloat16*>(q_lat), stream));
 }
 
-mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens, int B,
-                          int n_h, int max_seq_len, float softmax_scale, int num_splits, float* o_part,
-                          float* lse_part, int32_t* status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// mla_decode_fwd with the test hooks of DecodeParams (wait limit, withheld loads).
+mla_status decode_fwd_impl(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens, int B, int n_h,
+                           int max_seq_len, float softmax_scale, int num_splits, float* o_part, float* lse_part,
+                           int32_t* status, cudaStream_t stream, uint64_t wait_ns, int stall_loads) {
   if (!q_lat || !cache || !seq_lens || !o_part || !lse_part) return MLA_ERR_INVALID_ARG;
   if (!cache->data || cache->reserved != 0) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q_lat) || !aligned16(cache->data) || !aligned16(o_part) || !aligned16(lse_part) ||
@@ -160,10 +166,32 @@ mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32
     }
   }
   p.scale = softmax_scale;
+  p.wait_ns = wait_ns;
+  p.stall_loads = stall_loads;
   // TMA coordinates are 32-bit: a cache of 2^31 rows (over 1 TB) is not served.
   if (!decode_tc_supported(p)) return MLA_ERR_UNSUPPORTED;
   return cuda_status(p.kv_dtype == MLA_KV_BF16 ? launch_decode_tc(p, max_seq_len, stream)
                                                : launch_decode_tc_fp8(p, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_fwd(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens, int B,
+                          int n_h, int max_seq_len, float softmax_scale, int num_splits, float* o_part,
+                          float* lse_part, int32_t* status, cudaStream_t stream) {
+  return decode_fwd_impl(q_lat, cache, seq_lens, B, n_h, max_seq_len, softmax_scale, num_splits, o_part, lse_part,
+                         status, stream, 0, 0);
+}
+
+mla_status mla_test_decode_stalled(const void* q_lat, const mla_cache* cache, const int32_t* seq_lens, int B,
+                                   int n_h, int max_seq_len, float softmax_scale, int num_splits, float* o_part,
+                                   float* lse_part, int32_t* status, uint64_t wait_ns, cudaStream_t stream) {
+  if (!cache || cache->dtype != MLA_KV_BF16 || !status) return MLA_ERR_INVALID_ARG;
+  if (wait_ns < 1000 || wait_ns > kDecodeWaitNs) return MLA_ERR_INVALID_ARG;
+  return decode_fwd_impl(q_lat, cache, seq_lens, B, n_h, max_seq_len, softmax_scale, num_splits, o_part, lse_part,
+                         status, stream, wait_ns, 1);
 }
 
 mla_status mla_combine(const float* o_part, const float* lse_part, int B, int num_splits, int n_h,

@@ -186,6 +186,27 @@ def attend_latent(q_lat, rows, scale=None):
 
 
 # ---------------------------------------------------------------------------------
+# Writing the cache ([A] §"长上下文推理的第一瓶颈": each token's hidden state is
+# down-projected to the latent c_KV, d_c = 512, and only that is cached; [A] §"解耦
+# RoPE 与 YaRN": a shared 64-wide key carries the position, rotated where it is made;
+# hidden size 5120, [A] §"8.1T token 预训练配置与 H800 成本账" and [B] §"计算设置").
+# ---------------------------------------------------------------------------------
+def cache_rows(h, w_dkv, w_kr, pos, base: float = ROPE_BASE) -> np.ndarray:
+    """Cache rows of new tokens, unrounded.
+
+    h      [T, d]     hidden states of the new tokens
+    w_dkv  [512, d]   down-projection to the latent:  c_t = W_DKV · h_t
+    w_kr   [64, d]    projection to the shared RoPE key: k^R_t = RoPE(W_KR · h_t, pos_t)
+    pos    [T]        each token's position in its sequence
+    Returns [T, 576] = [c_t ‖ k^R_t].
+    """
+    h = _f64(h)
+    c = h @ _f64(w_dkv).T                                 # [T, 512]
+    k_raw = h @ _f64(w_kr).T                              # [T, 64]
+    return np.concatenate([c, rope(k_raw, _f64(pos), base)], axis=-1)
+
+
+# ---------------------------------------------------------------------------------
 # Log-sum-exp merge of attention over disjoint token subsets. The exact identity:
 # for a partition of the tokens into parts j with normalised outputs o_j and
 # log-normalisers lse_j,  lse = ln sum_j exp(lse_j)  and  o = sum_j exp(lse_j - lse) o_j.

@@ -1,4 +1,4 @@
-"""The C-ABI library without a GPU: it loads, exports every symbol include/mla.h
+"""The C-ABI library without a GPU: it loads, exports every symbol include/*.h
 declares, and rejects bad arguments on the host before touching CUDA."""
 
 import ctypes
@@ -17,8 +17,12 @@ MIS = A + 4          # misaligned
 
 
 def _declared():
-    hdr = open(os.path.join(ROOT, "include", "mla.h")).read()
-    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", hdr)))
+    names = set()
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            hdr = open(os.path.join(ROOT, "include", f)).read()
+            names.update(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", hdr))
+    return sorted(names)
 
 
 def test_library_exports_every_declared_symbol():
@@ -166,3 +170,18 @@ def test_tensors_on_two_devices_are_rejected():
         mla._one_device(q_lat=d0, o_part=d1)
     with pytest.raises(ValueError, match="cache.block_table"):
         mla._one_device(q_lat=d1, **{"cache.data": d1, "cache.block_table": d0})
+
+
+def test_stall_hook_rejects_bad_arguments_on_host():
+    L = _lib.get()
+
+    def stalled(c=None, status=A, wait_ns=2_000_000, **kw):
+        c = _cache() if c is None else c
+        return L.mla_test_decode_stalled(A, ctypes.byref(c), A, kw.get("B", 32), 128, 4096, 0.07, 2, A, A, status,
+                                         wait_ns, None)
+
+    assert stalled(status=None) == INVALID                          # the status word is where the timeout lands
+    assert stalled(_cache(dtype=1, scales=A)) == INVALID            # bf16 kernel only
+    assert stalled(wait_ns=10) == INVALID
+    assert stalled(wait_ns=3_000_000_000) == INVALID
+    assert stalled(B=0) == INVALID                                  # and every check of mla_decode_fwd

@@ -243,3 +243,71 @@ def test_cache_size_matches_the_pages():
                             g["avg_bits_per_element"]) / 1e9
     assert abs(b1 - g["cache_gb_batch1_printed"]) <= g["printed_precision_gb"]["batch1"]
     assert abs(b64 - g["cache_gb_batch64_printed"]) <= g["printed_precision_gb"]["batch64"]
+
+
+# ----------------------------- writing the cache ----------------------------------
+def _append_case(rng, T=4, d=96):
+    h = rng.standard_normal((T, d))
+    w_dkv = rng.standard_normal((512, d)) / math.sqrt(d)
+    w_kr = rng.standard_normal((64, d)) / math.sqrt(d)
+    return h, w_dkv, w_kr
+
+
+def test_cache_rows_of_basis_states_are_weight_columns():
+    # h = e_j: the latent is column j of W_DKV exactly; at position 0 the key is column j
+    # of W_KR unrotated, at position p it is that column turned by RoPE.
+    rng = np.random.default_rng(40)
+    _, w_dkv, w_kr = _append_case(rng)
+    for j in (0, 17, 95):
+        e = np.zeros((1, 96)); e[0, j] = 1.0
+        r0 = M.cache_rows(e, w_dkv, w_kr, [0])
+        np.testing.assert_array_equal(r0[0, :512], w_dkv[:, j])
+        np.testing.assert_array_equal(r0[0, 512:], w_kr[:, j])
+        r = M.cache_rows(e, w_dkv, w_kr, [777])
+        np.testing.assert_array_equal(r[0, :512], w_dkv[:, j])
+        np.testing.assert_allclose(r[0, 512:], M.rope(w_kr[:, j], 777), rtol=0, atol=1e-15)
+        assert not np.allclose(r[0, 512:], w_kr[:, j])
+
+
+def test_cache_rows_scalar_bruteforce():
+    rng = np.random.default_rng(41)
+    h, w_dkv, w_kr = _append_case(rng, T=2, d=8)
+    pos = [3, 40]
+    got = M.cache_rows(h, w_dkv, w_kr, pos)
+    for t in range(2):
+        for i in range(512):
+            assert got[t, i] == pytest.approx(sum(w_dkv[i, j] * h[t, j] for j in range(8)), rel=1e-12, abs=1e-14)
+        raw = [sum(w_kr[i, j] * h[t, j] for j in range(8)) for i in range(64)]
+        for i in range(32):
+            ang = pos[t] * 10000.0 ** (-i / 32.0)
+            assert got[t, 512 + i] == pytest.approx(raw[i] * math.cos(ang) - raw[i + 32] * math.sin(ang), abs=1e-12)
+            assert got[t, 544 + i] == pytest.approx(raw[i + 32] * math.cos(ang) + raw[i] * math.sin(ang), abs=1e-12)
+
+
+def test_written_keys_attend_by_relative_position():
+    # Rows written at positions t + delta, read by a query at L - 1 + delta: the
+    # attention result does not depend on delta, so each key is turned by its own
+    # position, the same way as the query.
+    rng = np.random.default_rng(42)
+    L, d = 6, 32
+    h, w_dkv, w_kr = _append_case(rng, T=L, d=d)
+    q, _, _, wk, wv = _rand_case(rng, n_h=2, L=L)
+    ref = None
+    for delta in (0, 9, 50000):
+        rows = M.cache_rows(h, w_dkv, w_kr, np.arange(L) + delta)
+        out = M.attend_explicit(q, rows[:, :512], rows[:, 512:], wk, wv, pos_q=L - 1 + delta)
+        if ref is None:
+            ref = out
+        else:
+            np.testing.assert_allclose(out["o"], ref["o"], rtol=1e-9, atol=1e-12)
+            np.testing.assert_allclose(out["lse"], ref["lse"], rtol=1e-9)
+
+
+def test_cache_rows_are_linear_in_the_hidden_state():
+    rng = np.random.default_rng(43)
+    h, w_dkv, w_kr = _append_case(rng, T=3)
+    h2 = rng.standard_normal(h.shape)
+    pos = [5, 6, 1000]
+    lhs = M.cache_rows(2.5 * h - h2, w_dkv, w_kr, pos)
+    rhs = 2.5 * M.cache_rows(h, w_dkv, w_kr, pos) - M.cache_rows(h2, w_dkv, w_kr, pos)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-10, atol=1e-12)

@@ -77,6 +77,12 @@ ORACLE_MUTANTS = [
     # cache-size arithmetic
     ("mla_cache_elements", "return (d_c + d_r) * layers", "return d_c * layers"),
     ("mha_cache_elements", "return 2 * n_h * d_h * layers", "return n_h * d_h * layers"),
+    # writing the cache: which weight, the key's rotation and its position
+    ("cache_rows", "c = h @ _f64(w_dkv).T", "c = h @ _f64(w_dkv).T * 1.0001"),
+    ("cache_rows", "rope(k_raw, _f64(pos), base)", "rope(k_raw, -_f64(pos), base)"),
+    ("cache_rows", "rope(k_raw, _f64(pos), base)", "rope(k_raw, _f64(pos) + 1, base)"),
+    ("cache_rows", "rope(k_raw, _f64(pos), base)", "k_raw"),
+    ("cache_rows", "k_raw = h @ _f64(w_kr).T", "k_raw = h @ _f64(w_dkv[:64]).T"),
 ]
 
 
