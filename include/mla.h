@@ -172,6 +172,34 @@ MLA_API mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h
                     float* o, cudaStream_t stream);
 
 /*
+ * mla_cache_append — write the cache rows of T new tokens.
+ *   ("DeepSeek-V2 机制拆解", §"长上下文推理的第一瓶颈": each token's hidden state is
+ *    down-projected to the cached latent c_KV, d_c = 512; §"解耦 RoPE 与 YaRN": the
+ *    shared 64-wide key carries the position, rotated where it is made; hidden size
+ *    5120: "中文验证版", §"计算设置".)
+ *   c_KV[t] = W_DKV h[t];  k^R[t] = RoPE(W_KR h[t], pos[t]) (the pairing of mla_absorb_q)
+ *   row[t]  = bf16([c_KV[t] ‖ k^R[t]]) stored as token pos[t] of sequence seq_ids[t]:
+ *     contiguous cache: row seq * seq_stride_tokens + pos
+ *     paged cache:      page block_table[seq, pos / 64], slot pos % 64
+ *   For an e4m3 cache the bf16 row is written to `staging` and then quantised as by
+ *   mla_quantize_fp8 into the cache's codes and scales at that row.
+ *   h        [T, d_model] bf16 (d_model a multiple of 512, at most 32768)
+ *   w_dkv    [512, d_model] bf16;  w_kr [64, d_model] bf16
+ *   seq_ids, pos  [T] int32 device
+ *   num_seqs sequences of the cache (rows of the block table, or contiguous sequences)
+ *   cache    the layer's cache; its rows (and scales) are WRITTEN
+ *   staging  [T, 576] bf16 device scratch, required for an e4m3 cache, else ignored
+ *   status   optional device word: MLA_ERR_DEVICE_BOUNDS for a token whose sequence,
+ *            position or page lies outside the cache (that token is not written)
+ *   T = 0 is a no-op. Two tokens with the same destination race (one of them wins).
+ */
+MLA_API mla_status mla_cache_append(const void* h, const void* w_dkv, const void* w_kr,
+                                    const int32_t* seq_ids, const int32_t* pos, int T,
+                                    int d_model, float rope_base, const mla_cache* cache,
+                                    int num_seqs, void* staging, int32_t* status,
+                                    cudaStream_t stream);
+
+/*
  * mla_quantize_fp8 — cache-write helper: bf16 rows → e4m3 rows + per-row scale.
  *   The pages report a low-bit KV cache for serving ("DeepSeek-V2 机制拆解",
  *   §"推理参数与 128K 上下文的使用注意"; "中文验证版", §"方法适配") without its format;

@@ -27,7 +27,8 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaEr
                    status_string)
 
 __all__ = [
-    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "num_splits", "split_range", "decode_kernel",
+    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "cache_append", "num_splits", "split_range",
+    "decode_kernel",
     "decode_combine_static",
     "compute_dtype",
     "Cache", "MlaError", "status_string", "default_scale", "decode_step", "DecodeStepGraph", "lib_path",
@@ -302,6 +303,33 @@ def up_v(o_lat, w_uv, o=None, stream=None):
     dev = _one_device(o_lat=o_lat, w_uv=w_uv, o=o)
     _call("mla_up_v", dev, _ptr(o_lat), _ptr(w_uv), B, n_h, _ptr(o), stream=stream)
     return o
+
+
+def cache_append(h, w_dkv, w_kr, seq_ids, pos, cache: Cache, num_seqs: int | None = None,
+                 rope_base: float = 10000.0, staging=None, status=None, stream=None):
+    """Write the cache rows of the new tokens (include/mla.h, mla_cache_append):
+    row = [W_DKV h ‖ RoPE(W_KR h, pos)] in bf16 at token pos[t] of sequence seq_ids[t].
+    h [T, d_model] bf16, w_dkv [512, d_model], w_kr [64, d_model] bf16, seq_ids/pos [T]
+    int32. An e4m3 cache needs (or gets allocated here) a bf16 staging buffer [T, 576]."""
+    T, d = h.shape[0], h.shape[1]
+    _need(h, "h", torch.bfloat16, (T, d))
+    _need(w_dkv, "w_dkv", torch.bfloat16, (D_LATENT, d))
+    _need(w_kr, "w_kr", torch.bfloat16, (D_ROPE, d))
+    _need(seq_ids, "seq_ids", torch.int32, (T,))
+    _need(pos, "pos", torch.int32, (T,))
+    if num_seqs is None:
+        num_seqs = cache.block_table.shape[0] if cache.block_table is not None else cache.data.shape[0]
+    if cache.dtype_code == MLA_KV_FP8_E4M3:
+        if staging is None:
+            staging = torch.empty(T, D_ROW, dtype=torch.bfloat16, device=h.device)
+        _need(staging, "staging", torch.bfloat16, (T, D_ROW))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    c = cache.to_c()
+    dev = _one_device(h=h, w_dkv=w_dkv, w_kr=w_kr, seq_ids=seq_ids, pos=pos, staging=staging, status=status,
+                      **cache.tensors())
+    _call("mla_cache_append", dev, _ptr(h), _ptr(w_dkv), _ptr(w_kr), _ptr(seq_ids), _ptr(pos), T, d,
+          float(rope_base), ctypes.byref(c), int(num_seqs), _ptr(staging), _ptr(status), stream=stream)
 
 
 def quantize_fp8(rows, codes=None, scales=None, stream=None):

@@ -26,7 +26,7 @@ MLA_STATIC_SCRATCH_BYTES = 64 << 20
 EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
     "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version", "mla_decode_kernel",
-    "mla_decode_combine_static", "mla_test_decode_stalled",
+    "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append",
 ]
 
 
@@ -65,6 +65,7 @@ def _load():
     lib.mla_test_decode_stalled.argtypes = [vp, ctypes.POINTER(MlaCache), vp, i32, i32, i32, f32, i32, vp, vp, vp,
                                             ctypes.c_uint64, vp]
     lib.mla_up_v.argtypes = [vp, vp, i32, i32, vp, vp]
+    lib.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, ctypes.POINTER(MlaCache), i32, vp, vp, vp]
     lib.mla_quantize_fp8.argtypes = [vp, i64, vp, vp, vp]
     lib.mla_num_splits.argtypes = [i32, i32, i32]
     lib.mla_decode_kernel.argtypes = [i32, i32]
@@ -73,7 +74,7 @@ def _load():
     lib.mla_status_string.restype = ctypes.c_char_p
     for fn in ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
                "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel",
-               "mla_decode_combine_static", "mla_test_decode_stalled"):
+               "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 

@@ -10,12 +10,8 @@
 // tcgen05 accumulates four 128 x N fp32 tiles in TMEM and the epilogue rounds them to
 // bf16. The weight bytes dominate: W_UK is read from HBM once per call.
 //
-// The decoupled part is rotated on CUDA cores. Pair (i, i + 32) turns by
-// theta_i = pos * base^(-2i/64); positions reach 131071, where an fp32 product would
-// be off by ~1e-2 rad, so the angle is reduced exactly: f_i = base^(-2i/64) / (2 pi) is
-// held as a 64-bit fixed-point fraction (computed on the host in double), the turn
-// count's fraction is the wrapping 64-bit product pos * f_i, and only the reduced angle
-// goes through fp32 sincos.
+// The decoupled part is rotated on CUDA cores with the exactly reduced angles of
+// rope.cuh.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -23,6 +19,7 @@
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "rope.cuh"
 #include "tmap.cuh"
 
 namespace mla {
@@ -38,10 +35,6 @@ constexpr int OFF_Q = 4 * kWTile;            // q^C tile: two 64-d chunks x 128 
 constexpr int OFF_BAR = OFF_Q + 2 * kNB * 128;
 constexpr int kSmem = OFF_BAR + 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
-
-struct RopeTurns {
-  unsigned long long f[kRope / 2];   // base^(-2i/64) / (2 pi) as an unsigned 0.64 fixed-point fraction
-};
 
 __global__ void __launch_bounds__(kThreads, 1)
 absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
@@ -120,7 +113,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
         const int64_t row = (int64_t)(b0 + n) * n_h + h;
         const uint4 u1 = *reinterpret_cast<const uint4*>(q + row * kQ + kNope + 8 * g);
         const uint4 u2 = *reinterpret_cast<const uint4*>(q + row * kQ + kNope + kRope / 2 + 8 * g);
-        const unsigned long long ps = (unsigned long long)(long long)pos[b0 + n];
+        const int ps = pos[b0 + n];
         const __nv_bfloat162* x1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
         const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&u2);
         uint32_t o1[4], o2[4];
@@ -131,10 +124,8 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int i = 8 * g + 2 * e + k;
-            const unsigned long long frac = ps * turns.f[i];
-            const float ang = (float)(frac >> 40) * (6.283185307179586f / 16777216.f);
             float sn, cs;
-            sincosf(ang, &sn, &cs);
+            rope_sincos(ps, turns.f[i], &sn, &cs);
             const float y1 = k ? a1.y : a1.x, y2 = k ? a2.y : a2.x;
             r1[k] = y1 * cs - y2 * sn;
             r2[k] = y2 * cs + y1 * sn;
@@ -179,23 +170,6 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 512);
-}
-
-// Fixed-point turns per position of the 32 RoPE frequencies of `base` (2^64 units of a
-// full turn), computed once per base.
-RopeTurns rope_turns(float rope_base) {
-  static std::mutex mu;
-  static float last_base = 0.f;
-  static RopeTurns last;
-  std::lock_guard<std::mutex> lock(mu);
-  if (rope_base != last_base) {
-    for (int i = 0; i < kRope / 2; ++i) {
-      const double f = std::pow((double)rope_base, -2.0 * i / (double)kRope) / (2.0 * M_PI);   // < 1/(2 pi)
-      last.f[i] = (unsigned long long)std::ldexp(f, 64);
-    }
-    last_base = rope_base;
-  }
-  return last;
 }
 
 }  // namespace

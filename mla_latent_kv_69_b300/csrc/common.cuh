@@ -88,6 +88,10 @@ cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, in
                         cudaStream_t st);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int S, int n_h,
                            float* o_lat, float* lse, cudaStream_t st);
+cudaError_t launch_cache_append(const __nv_bfloat16* h, const __nv_bfloat16* w_dkv, const __nv_bfloat16* w_kr,
+                                const int32_t* seq_ids, const int32_t* pos, int T, int d, float rope_base,
+                                const mla_cache& cache, int num_seqs, __nv_bfloat16* staging, int32_t* status,
+                                cudaStream_t st);
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t n, uint8_t* codes, float* scales,
                                 cudaStream_t st);
 

@@ -212,6 +212,37 @@ mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h, float*
   return cuda_status(launch_up_v(o_lat, static_cast<const __nv_bfloat16*>(w_uv), B, n_h, o, stream));
 }
 
+mla_status mla_cache_append(const void* h, const void* w_dkv, const void* w_kr, const int32_t* seq_ids,
+                            const int32_t* pos, int T, int d_model, float rope_base, const mla_cache* cache,
+                            int num_seqs, void* staging, int32_t* status, cudaStream_t stream) {
+  if (!h || !w_dkv || !w_kr || !seq_ids || !pos || !cache || !cache->data) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(cache->data) || !aligned16(seq_ids) ||
+      !aligned16(pos))
+    return MLA_ERR_INVALID_ARG;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (T < 0 || T > kMaxBatch * 128) return MLA_ERR_INVALID_ARG;
+  if (d_model < 512 || d_model > 32768 || d_model % 512) return d_model > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (!(rope_base > 1.f) || !std::isfinite(rope_base)) return MLA_ERR_INVALID_ARG;
+  if (num_seqs < 1 || cache->reserved != 0 || cache->num_rows < 1) return MLA_ERR_INVALID_ARG;
+  if (cache->dtype == MLA_KV_BF16) {
+    if (cache->scales) return MLA_ERR_INVALID_ARG;
+  } else if (cache->dtype == MLA_KV_FP8_E4M3) {
+    if (!cache->scales || !aligned16(cache->scales) || !staging || !aligned16(staging)) return MLA_ERR_INVALID_ARG;
+  } else {
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (cache->block_table) {
+    if (cache->page_size != kPage) return cache->page_size > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+    if (!aligned16(cache->block_table) || cache->max_pages < 1 || cache->num_rows % kPage) return MLA_ERR_INVALID_ARG;
+  } else if (cache->seq_stride_tokens < 1) {
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (T == 0) return MLA_OK;
+  return cuda_status(launch_cache_append(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(w_dkv),
+                                         static_cast<const __nv_bfloat16*>(w_kr), seq_ids, pos, T, d_model, rope_base,
+                                         *cache, num_seqs, static_cast<__nv_bfloat16*>(staging), status, stream));
+}
+
 mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t* codes, float* scales,
                             cudaStream_t stream) {
   if (!rows || !codes || !scales) return MLA_ERR_INVALID_ARG;

@@ -468,6 +468,21 @@ namespace sm100 {
 // Order this thread's earlier memory operations (including stores to a peer CTA's shared
 // memory) before its later ones, at cluster scope.
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// A 32-bit word from any CTA's shared memory (a shared::cluster address from mapa).
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+  return v;
+}
+// Four fp32 from any CTA's shared memory (a shared::cluster address from mapa).
+__device__ __forceinline__ float4 ld_cluster_v4_f32(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_cluster_v2_f32(uint32_t caddr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(caddr), "f"(a), "f"(b) : "memory");
 }

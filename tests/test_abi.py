@@ -185,3 +185,28 @@ def test_stall_hook_rejects_bad_arguments_on_host():
     assert stalled(wait_ns=10) == INVALID
     assert stalled(wait_ns=3_000_000_000) == INVALID
     assert stalled(B=0) == INVALID                                  # and every check of mla_decode_fwd
+
+
+def test_cache_append_rejects_bad_arguments_on_host():
+    L = _lib.get()
+
+    def append(c=None, h=A, T=4, d=5120, base=10000.0, num_seqs=32, staging=None, status=None):
+        c = _cache() if c is None else c
+        return L.mla_cache_append(h, A, A, A, A, T, d, base, ctypes.byref(c), num_seqs, staging, status, None)
+
+    assert append(T=0) == _lib.MLA_OK                              # nothing to write
+    assert append(h=None) == INVALID
+    assert append(h=MIS) == INVALID
+    assert append(T=-1) == INVALID
+    assert append(d=5000) == UNSUPPORTED                           # not a multiple of 512
+    assert append(d=0) == INVALID
+    assert append(base=0.5) == INVALID
+    assert append(num_seqs=0) == INVALID
+    assert append(status=A + 2) == INVALID
+    assert append(_cache(dtype=1, scales=A)) == INVALID             # e4m3 needs the staging buffer
+    assert append(_cache(dtype=1)) == INVALID                       # ... and scales
+    assert append(_cache(scales=A)) == INVALID                      # bf16 with scales
+    assert append(_cache(seq_stride_tokens=0)) == INVALID
+    paged = dict(block_table=A, page_size=64, max_pages=64, num_rows=64 * 100)
+    assert append(_cache(**{**paged, "page_size": 16})) == UNSUPPORTED
+    assert append(_cache(**{**paged, "num_rows": 64 * 100 + 1})) == INVALID

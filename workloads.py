@@ -37,6 +37,8 @@ D_Q = 192
 PAGE = 64
 
 TAG_Q, TAG_ROWS, TAG_WUK, TAG_WUV, TAG_LENS, TAG_PAGES, TAG_QLAT = 1, 2, 3, 4, 5, 6, 7
+TAG_H, TAG_WDKV, TAG_WKR = 8, 9, 10
+D_MODEL = 5120   # hidden size ([A] §"8.1T token 预训练配置与 H800 成本账"; [B] §"计算设置")
 
 
 @dataclass(frozen=True)
@@ -122,6 +124,21 @@ def gen_w_uk(w: Workload) -> np.ndarray:
 
 def gen_w_uv(w: Workload) -> np.ndarray:
     return _normal_bf16(stream(w.seed, TAG_WUV), (w.n_h, D_NOPE, D_LATENT), std=1.0 / np.sqrt(512.0))
+
+
+def gen_hidden(seed: int, T: int, d: int = D_MODEL) -> np.ndarray:
+    """bf16 bits [T, d], N(0, 1): hidden states of new tokens (the cache write's input)."""
+    return _normal_bf16(stream(seed, TAG_H), (T, d))
+
+
+def gen_w_dkv(seed: int, d: int = D_MODEL) -> np.ndarray:
+    """bf16 bits [512, d], N(0, 1/d): the down-projection to the latent."""
+    return _normal_bf16(stream(seed, TAG_WDKV), (D_LATENT, d), std=1.0 / np.sqrt(d))
+
+
+def gen_w_kr(seed: int, d: int = D_MODEL) -> np.ndarray:
+    """bf16 bits [64, d], N(0, 1/d): the projection to the shared RoPE key."""
+    return _normal_bf16(stream(seed, TAG_WKR), (D_ROPE, d), std=1.0 / np.sqrt(d))
 
 
 def gen_rows(w: Workload, b: int, length: int) -> np.ndarray:
