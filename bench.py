@@ -414,6 +414,32 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     eager_mean = dist.max(float(np.mean(eager_ms)), dev)
     del g
 
+    # The cache write of the step's new tokens (mla_cache_append): one token per
+    # sequence, hidden size 5120, written over each sequence's newest row.
+    d_model = W.D_MODEL
+    h_new = W.bits_to_torch_bf16(W.gen_hidden(w.seed, B, d_model), dev)
+    w_dkv = W.bits_to_torch_bf16(W.gen_w_dkv(w.seed, d_model), dev)
+    w_kr = W.bits_to_torch_bf16(W.gen_w_kr(w.seed, d_model), dev)
+    a_seq = torch.arange(B, dtype=torch.int32, device=dev)
+    a_pos = torch.clamp(case.seq_lens - 1, min=0)
+    a_stage = torch.empty(B, 576, dtype=torch.bfloat16, device=dev) if w.kv == "fp8" else None
+    for _ in range(3):
+        mla.cache_append(h_new, w_dkv, w_kr, a_seq, a_pos, cache, staging=a_stage)
+    torch.cuda.synchronize()
+    app_ms = []
+    for _ in range(K):
+        flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        mla.cache_append(h_new, w_dkv, w_kr, a_seq, a_pos, cache, staging=a_stage)
+        b.record(stream)
+        b.synchronize()
+        app_ms.append(a.elapsed_time(b))
+    app_mean = float(np.mean(app_ms))
+    row_bytes = 576 * 2 if w.kv == "bf16" else 576 + 4 + 2 * 576 * 2   # e4m3: codes + scale, staging out and in
+    app_bytes = 576 * d_model * 2 + B * d_model * 2 + B * row_bytes
+    del h_new, w_dkv, w_kr, a_seq, a_pos, a_stage
+
     peaks, peaks_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     total_cache = dist.sum(cache_bytes, dev)
@@ -464,22 +490,28 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         "decode_kernel": mla.decode_kernel(w.kv, n_h),
         "roofline": roofline,
         "cache_gbs_decode_combine": round(cache_bytes / ((decode_ms + float(kern_ms[2])) / 1e3) / 1e9, 1),
-        "e2e": {"value": round(total_cache / (e2e_mean / 1e3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_mean, 5), "host_ms_per_step": round(float(np.mean(host_ms)), 4),
-                "steps": len(e2e_ms), "ms_median": round(float(np.median(e2e_ms)), 5),
-                "ms_max": round(float(np.max(e2e_ms)), 5),
-                "device_step_ratio": round(e2e_mean / step_ms, 2),
+        "e2e": {"value": round(total_cache / (eager_mean / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(eager_mean, 5), "host_ms_per_step": round(float(np.mean(eager_host_ms)), 4),
+                "steps": len(eager_ms), "ms_median": round(float(np.median(eager_ms)), 5),
+                "ms_max": round(float(np.max(eager_ms)), 5),
+                "device_step_ratio": round(eager_mean / step_ms, 2),
                 "h2d_bytes_per_step": int(h_q.numel() * 2 + h_pos.numel() * 4 + h_len.numel() * 4),
                 "d2h_bytes_per_step": int(h_o.numel() * 4),
-                "path": "mla.DecodeStepGraph.replay (the step captured once over the C ABI: H2D of q, pos and "
-                        "seq_lens from pinned host buffers, the four calls, D2H of o)",
-                "same_o_as_eager": same_o,
-                "eager": {"value": round(total_cache / (eager_mean / 1e3) / 1e9, 2), "unit": "GB/s",
-                          "ms_per_step": round(eager_mean, 5),
-                          "host_ms_per_step": round(float(np.mean(eager_host_ms)), 4),
-                          "ms_median": round(float(np.median(eager_ms)), 5),
-                          "path": "mla.decode_step (four Python calls over the C ABI each step) with the same "
-                                  "pinned host buffers and copies"}},
+                "path": "mla.decode_step (four Python calls over the C ABI) with H2D of q, pos and seq_lens from "
+                        "pinned host buffers and D2H of o into a pinned buffer, every step",
+                "same_o_as_graph": same_o,
+                "graph": {"value": round(total_cache / (e2e_mean / 1e3) / 1e9, 2), "unit": "GB/s",
+                          "ms_per_step": round(e2e_mean, 5),
+                          "host_ms_per_step": round(float(np.mean(host_ms)), 4),
+                          "ms_median": round(float(np.median(e2e_ms)), 5),
+                          "path": "mla.DecodeStepGraph.replay: the same copies and calls captured once"}},
+        "cache_append": {"ms": round(app_mean, 5), "tokens": B, "d_model": d_model,
+                         "algorithmic_bytes": int(app_bytes),
+                         "achieved_gbs": round(app_bytes / (app_mean / 1e3) / 1e9, 1),
+                         "frac": round(app_bytes / (app_mean / 1e3) / 1e9 / hbm_peak, 4),
+                         "bound": "hbm", "peak_gbs": hbm_peak,
+                         "note": "W_DKV and W_KR read once, the new tokens' hidden states and rows; "
+                                 "CUDA events around one call, L2 flushed before each"},
         "clocks": {**clocks, "window": f"{args.soak:.1f} s soak + the timed steps"},
     }
     del case, cache, bufs, e2e_bufs, flush, drain, graph, graph_parts

@@ -116,6 +116,35 @@ MLA_API mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* 
                         cudaStream_t stream);
 
 /*
+ * RoPE of the decoupled query and key, for the _ex entry points.
+ *   ("DeepSeek-V2 机制拆解", §"解耦 RoPE 与 YaRN": the 128K context comes from YaRN on
+ *    the decoupled shared key, scale 40, alpha 1, beta 32, target 160K; "中文验证版",
+ *    §"计算设置": pre-training length 4K. The pages give no formula; this follows the
+ *    published YaRN frequency rule.)
+ *   Pair i's frequency is theta_i = base^(-i/32) (plain RoPE, yarn_scale = 1), or with
+ *   YaRN, from the turns r_i = original_max_pos * theta_i / (2 pi) the pair makes over
+ *   the original context: theta_i when r_i >= yarn_beta, theta_i / yarn_scale when
+ *   r_i <= yarn_alpha, and (1 - g) theta_i / yarn_scale + g theta_i with
+ *   g = (r_i - yarn_alpha) / (yarn_beta - yarn_alpha) in between. YaRN's attention
+ *   temperature is the caller's softmax_scale (mla_decode_fwd). The pages' setting:
+ *   {10000, 40, 1, 32, 4096, 0}.
+ */
+typedef struct mla_rope {
+  float base;                   /* > 1                                              */
+  float yarn_scale;             /* 1: plain RoPE; > 1: YaRN                          */
+  float yarn_alpha;             /* YaRN: 0 <= alpha < beta (turns over the context)  */
+  float yarn_beta;
+  int32_t original_max_pos;     /* YaRN: the original context length (>= 1)          */
+  int32_t reserved;             /* must be 0                                         */
+} mla_rope;
+
+/* mla_absorb_q with the RoPE of `rope` (host struct) instead of plain RoPE of base
+ * rope_base. mla_absorb_q(..., base, ...) equals this with {base, 1, 0, 0, 0, 0}. */
+MLA_API mla_status mla_absorb_q_ex(const void* q, const void* w_uk, const int32_t* pos,
+                                   int B, int n_h, const mla_rope* rope, void* q_lat,
+                                   cudaStream_t stream);
+
+/*
  * mla_decode_fwd — split-KV attention of all heads over the latent cache.
  *   Scores s[h,t] = softmax_scale * (q_lat[b,h,:] . row_t[0:576]), softmax over
  *   the tokens of each split with a running maximum, and the value is the latent
@@ -198,6 +227,13 @@ MLA_API mla_status mla_cache_append(const void* h, const void* w_dkv, const void
                                     int d_model, float rope_base, const mla_cache* cache,
                                     int num_seqs, void* staging, int32_t* status,
                                     cudaStream_t stream);
+
+/* mla_cache_append with the RoPE of `rope` (see mla_rope) for the shared key. */
+MLA_API mla_status mla_cache_append_ex(const void* h, const void* w_dkv, const void* w_kr,
+                                       const int32_t* seq_ids, const int32_t* pos, int T,
+                                       int d_model, const mla_rope* rope,
+                                       const mla_cache* cache, int num_seqs, void* staging,
+                                       int32_t* status, cudaStream_t stream);
 
 /*
  * mla_quantize_fp8 — cache-write helper: bf16 rows → e4m3 rows + per-row scale.

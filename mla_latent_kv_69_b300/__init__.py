@@ -23,7 +23,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaError, check,
+from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaError, MlaRope, check,
                    status_string)
 
 __all__ = [
@@ -31,7 +31,7 @@ __all__ = [
     "decode_kernel",
     "decode_combine_static",
     "compute_dtype",
-    "Cache", "MlaError", "status_string", "default_scale", "decode_step", "DecodeStepGraph", "lib_path",
+    "Cache", "Yarn", "MlaError", "status_string", "default_scale", "decode_step", "DecodeStepGraph", "lib_path",
     "MLA_MAX_SPLITS", "test_decode_stalled",
 ]
 
@@ -108,6 +108,27 @@ def _need_table_rows(cache, B):
     bt = cache.block_table
     if bt is not None and (bt.dim() != 2 or bt.shape[0] < B):
         raise ValueError(f"block_table must have a row per sequence: [>= {B}, max_pages]")
+
+
+@dataclass(frozen=True)
+class Yarn:
+    """YaRN extension of the decoupled RoPE (mla_rope in include/mla.h); the defaults are
+    the pages' setting over a 4K pre-training context."""
+    scale: float = 40.0
+    alpha: float = 1.0
+    beta: float = 32.0
+    original_max_pos: int = 4096
+
+
+def _rope(rope_base: float, yarn: Yarn | None) -> MlaRope:
+    r = MlaRope()
+    r.base = float(rope_base)
+    r.yarn_scale = 1.0 if yarn is None else float(yarn.scale)
+    r.yarn_alpha = 0.0 if yarn is None else float(yarn.alpha)
+    r.yarn_beta = 0.0 if yarn is None else float(yarn.beta)
+    r.original_max_pos = 0 if yarn is None else int(yarn.original_max_pos)
+    r.reserved = 0
+    return r
 
 
 @dataclass
@@ -193,7 +214,7 @@ def split_range(seq_len: int, n_splits: int, split: int) -> tuple[int, int]:
     return a.value, b.value
 
 
-def absorb_q(q, w_uk, pos, q_lat=None, rope_base: float = 10000.0, stream=None):
+def absorb_q(q, w_uk, pos, q_lat=None, rope_base: float = 10000.0, stream=None, yarn: Yarn | None = None):
     B, n_h = q.shape[0], q.shape[1]
     _need(q, "q", torch.bfloat16, (B, n_h, D_Q))
     _need(w_uk, "w_uk", torch.bfloat16, (n_h, D_NOPE, D_LATENT))
@@ -202,7 +223,13 @@ def absorb_q(q, w_uk, pos, q_lat=None, rope_base: float = 10000.0, stream=None):
         q_lat = torch.empty(B, n_h, D_ROW, dtype=torch.bfloat16, device=q.device)
     _need(q_lat, "q_lat", torch.bfloat16, (B, n_h, D_ROW))
     dev = _one_device(q=q, w_uk=w_uk, pos=pos, q_lat=q_lat)
-    _call("mla_absorb_q", dev, _ptr(q), _ptr(w_uk), _ptr(pos), B, n_h, float(rope_base), _ptr(q_lat), stream=stream)
+    if yarn is None:
+        _call("mla_absorb_q", dev, _ptr(q), _ptr(w_uk), _ptr(pos), B, n_h, float(rope_base), _ptr(q_lat),
+              stream=stream)
+    else:
+        r = _rope(rope_base, yarn)
+        _call("mla_absorb_q_ex", dev, _ptr(q), _ptr(w_uk), _ptr(pos), B, n_h, ctypes.byref(r), _ptr(q_lat),
+              stream=stream)
     return q_lat
 
 
@@ -306,7 +333,7 @@ def up_v(o_lat, w_uv, o=None, stream=None):
 
 
 def cache_append(h, w_dkv, w_kr, seq_ids, pos, cache: Cache, num_seqs: int | None = None,
-                 rope_base: float = 10000.0, staging=None, status=None, stream=None):
+                 rope_base: float = 10000.0, staging=None, status=None, stream=None, yarn: Yarn | None = None):
     """Write the cache rows of the new tokens (include/mla.h, mla_cache_append):
     row = [W_DKV h ‖ RoPE(W_KR h, pos)] in bf16 at token pos[t] of sequence seq_ids[t].
     h [T, d_model] bf16, w_dkv [512, d_model], w_kr [64, d_model] bf16, seq_ids/pos [T]
@@ -328,8 +355,9 @@ def cache_append(h, w_dkv, w_kr, seq_ids, pos, cache: Cache, num_seqs: int | Non
     c = cache.to_c()
     dev = _one_device(h=h, w_dkv=w_dkv, w_kr=w_kr, seq_ids=seq_ids, pos=pos, staging=staging, status=status,
                       **cache.tensors())
-    _call("mla_cache_append", dev, _ptr(h), _ptr(w_dkv), _ptr(w_kr), _ptr(seq_ids), _ptr(pos), T, d,
-          float(rope_base), ctypes.byref(c), int(num_seqs), _ptr(staging), _ptr(status), stream=stream)
+    r = _rope(rope_base, yarn)
+    _call("mla_cache_append_ex", dev, _ptr(h), _ptr(w_dkv), _ptr(w_kr), _ptr(seq_ids), _ptr(pos), T, d,
+          ctypes.byref(r), ctypes.byref(c), int(num_seqs), _ptr(staging), _ptr(status), stream=stream)
 
 
 def quantize_fp8(rows, codes=None, scales=None, stream=None):
@@ -352,10 +380,10 @@ def quantize_fp8(rows, codes=None, scales=None, stream=None):
 
 def decode_step(q, w_uk, w_uv, cache: Cache, seq_lens, pos, max_seq_len: int, n_splits: int = 0,
                 softmax_scale: float | None = None, rope_base: float = 10000.0, bufs: dict | None = None,
-                status=None, stream=None):
+                status=None, stream=None, yarn: Yarn | None = None):
     """All four calls of one decode step; `bufs` (optional) holds preallocated outputs."""
     bufs = {} if bufs is None else bufs
-    q_lat = absorb_q(q, w_uk, pos, q_lat=bufs.get("q_lat"), rope_base=rope_base, stream=stream)
+    q_lat = absorb_q(q, w_uk, pos, q_lat=bufs.get("q_lat"), rope_base=rope_base, stream=stream, yarn=yarn)
     o_part, lse_part = decode_fwd(q_lat, cache, seq_lens, max_seq_len, softmax_scale, n_splits,
                                   o_part=bufs.get("o_part"), lse_part=bufs.get("lse_part"), status=status,
                                   stream=stream)
@@ -383,7 +411,8 @@ class DecodeStepGraph:
     """
 
     def __init__(self, w_uk, w_uv, cache: Cache, B: int, max_seq_len: int, n_splits: int = 0,
-                 softmax_scale: float | None = None, rope_base: float = 10000.0, status=None):
+                 softmax_scale: float | None = None, rope_base: float = 10000.0, status=None,
+                 yarn: Yarn | None = None):
         n_h = w_uk.shape[0]
         dev = w_uk.device
         self.device, self.B, self.n_h = dev, B, n_h
@@ -405,7 +434,8 @@ class DecodeStepGraph:
         self.stream = torch.cuda.Stream(dev)
         self.graph = torch.cuda.CUDAGraph()
         args = (w_uk, w_uv, cache, self.d_seq_lens, self.d_pos, max_seq_len)
-        kw = dict(n_splits=n_splits, softmax_scale=softmax_scale, rope_base=rope_base, bufs=self.bufs, status=status)
+        kw = dict(n_splits=n_splits, softmax_scale=softmax_scale, rope_base=rope_base, bufs=self.bufs, status=status,
+                  yarn=yarn)
         with torch.cuda.device(dev), torch.cuda.stream(self.stream):
             # one eager step first: every argument check and launch path runs once outside capture
             decode_step(self.d_q, *args, **kw)

@@ -26,7 +26,8 @@ MLA_STATIC_SCRATCH_BYTES = 64 << 20
 EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
     "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version", "mla_decode_kernel",
-    "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append",
+    "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append", "mla_absorb_q_ex",
+    "mla_cache_append_ex",
 ]
 
 
@@ -41,6 +42,17 @@ class MlaCache(ctypes.Structure):
         ("reserved", ctypes.c_int32),
         ("seq_stride_tokens", ctypes.c_int64),
         ("num_rows", ctypes.c_int64),
+    ]
+
+
+class MlaRope(ctypes.Structure):
+    _fields_ = [
+        ("base", ctypes.c_float),
+        ("yarn_scale", ctypes.c_float),
+        ("yarn_alpha", ctypes.c_float),
+        ("yarn_beta", ctypes.c_float),
+        ("original_max_pos", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -66,6 +78,9 @@ def _load():
                                             ctypes.c_uint64, vp]
     lib.mla_up_v.argtypes = [vp, vp, i32, i32, vp, vp]
     lib.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, ctypes.POINTER(MlaCache), i32, vp, vp, vp]
+    lib.mla_cache_append_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, ctypes.POINTER(MlaRope),
+                                        ctypes.POINTER(MlaCache), i32, vp, vp, vp]
+    lib.mla_absorb_q_ex.argtypes = [vp, vp, vp, i32, i32, ctypes.POINTER(MlaRope), vp, vp]
     lib.mla_quantize_fp8.argtypes = [vp, i64, vp, vp, vp]
     lib.mla_num_splits.argtypes = [i32, i32, i32]
     lib.mla_decode_kernel.argtypes = [i32, i32]
@@ -74,7 +89,8 @@ def _load():
     lib.mla_status_string.restype = ctypes.c_char_p
     for fn in ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
                "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel",
-               "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append"):
+               "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append", "mla_absorb_q_ex",
+               "mla_cache_append_ex"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 

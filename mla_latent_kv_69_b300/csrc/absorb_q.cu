@@ -175,7 +175,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
 }  // namespace
 
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const int32_t* pos,
-                            int B, int n_h, float rope_base, __nv_bfloat16* q_lat, cudaStream_t st) {
+                            int B, int n_h, const RopeSpec& rope, __nv_bfloat16* q_lat, cudaStream_t st) {
   // W_UK viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = one M-tile (2 chunks)
   CUtensorMap wmap, qmap;
   {
@@ -197,7 +197,7 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, c
                       &qmap))
       return cudaErrorInvalidValue;
   }
-  const RopeTurns turns = rope_turns(rope_base);
+  const RopeTurns turns = rope_turns(rope);
   static std::atomic<int> attr_done[kMaxDevices];
   const cudaError_t attr_err = smem_attr_once(absorb_q_tc, kSmem, attr_done);
   if (attr_err != cudaSuccess) return attr_err;

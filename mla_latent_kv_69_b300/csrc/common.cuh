@@ -81,15 +81,21 @@ __device__ inline int64_t cache_row(const DecodeParams& p, int b, int t) {
   return row;
 }
 
+// RoPE frequencies of the decoupled query/key (mla_rope in include/mla.h, validated).
+struct RopeSpec {
+  double base, yarn_scale, yarn_alpha, yarn_beta;
+  int32_t original_max_pos;
+};
+
 // Host-side launchers (one per kernel family); each returns the launch error.
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const int32_t* pos,
-                            int B, int n_h, float rope_base, __nv_bfloat16* q_lat, cudaStream_t st);
+                            int B, int n_h, const RopeSpec& rope, __nv_bfloat16* q_lat, cudaStream_t st);
 cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, int n_h, float* o,
                         cudaStream_t st);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int S, int n_h,
                            float* o_lat, float* lse, cudaStream_t st);
 cudaError_t launch_cache_append(const __nv_bfloat16* h, const __nv_bfloat16* w_dkv, const __nv_bfloat16* w_kr,
-                                const int32_t* seq_ids, const int32_t* pos, int T, int d, float rope_base,
+                                const int32_t* seq_ids, const int32_t* pos, int T, int d, const RopeSpec& rope,
                                 const mla_cache& cache, int num_seqs, __nv_bfloat16* staging, int32_t* status,
                                 cudaStream_t st);
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t n, uint8_t* codes, float* scales,

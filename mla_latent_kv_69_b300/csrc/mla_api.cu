@@ -40,6 +40,21 @@ int sm_count() {
   return cached[dev];
 }
 
+// A validated mla_rope: base > 1; plain (yarn_scale = 1) or YaRN with scale > 1,
+// 0 <= alpha < beta and original_max_pos >= 1.
+bool rope_spec(const mla_rope* r, RopeSpec* out) {
+  if (!r || r->reserved != 0) return false;
+  if (!(r->base > 1.f) || !std::isfinite(r->base)) return false;
+  if (!(r->yarn_scale >= 1.f) || !std::isfinite(r->yarn_scale)) return false;
+  if (r->yarn_scale > 1.f) {
+    if (!(r->yarn_alpha >= 0.f) || !(r->yarn_beta > r->yarn_alpha) || !std::isfinite(r->yarn_beta)) return false;
+    if (r->original_max_pos < 1) return false;
+  }
+  *out = RopeSpec{(double)r->base, (double)r->yarn_scale, (double)r->yarn_alpha, (double)r->yarn_beta,
+                  r->original_max_pos};
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -84,13 +99,20 @@ int mla_num_splits(int B, int max_seq_len, int n_h) {
 
 mla_status mla_absorb_q(const void* q, const void* w_uk, const int32_t* pos, int B, int n_h,
                         float rope_base, void* q_lat, cudaStream_t stream) {
+  const mla_rope r = {rope_base, 1.f, 0.f, 0.f, 0, 0};
+  return mla_absorb_q_ex(q, w_uk, pos, B, n_h, &r, q_lat, stream);
+}
+
+mla_status mla_absorb_q_ex(const void* q, const void* w_uk, const int32_t* pos, int B, int n_h,
+                           const mla_rope* rope, void* q_lat, cudaStream_t stream) {
   if (!q || !w_uk || !pos || !q_lat) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(w_uk) || !aligned16(q_lat) || !aligned16(pos)) return MLA_ERR_INVALID_ARG;
   if (B < 1 || B > kMaxBatch) return MLA_ERR_INVALID_ARG;
   if (!valid_heads(n_h)) return n_h > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
-  if (!(rope_base > 1.f) || !std::isfinite(rope_base)) return MLA_ERR_INVALID_ARG;
+  RopeSpec spec;
+  if (!rope_spec(rope, &spec)) return MLA_ERR_INVALID_ARG;
   return cuda_status(launch_absorb_q(static_cast<const __nv_bfloat16*>(q),
-                                     static_cast<const __nv_bfloat16*>(w_uk), pos, B, n_h, rope_base,
+                                     static_cast<const __nv_bfloat16*>(w_uk), pos, B, n_h, spec,
                                      static_cast<__nv_bfloat16*>(q_lat), stream));
 }
 
@@ -215,6 +237,13 @@ mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h, float*
 mla_status mla_cache_append(const void* h, const void* w_dkv, const void* w_kr, const int32_t* seq_ids,
                             const int32_t* pos, int T, int d_model, float rope_base, const mla_cache* cache,
                             int num_seqs, void* staging, int32_t* status, cudaStream_t stream) {
+  const mla_rope r = {rope_base, 1.f, 0.f, 0.f, 0, 0};
+  return mla_cache_append_ex(h, w_dkv, w_kr, seq_ids, pos, T, d_model, &r, cache, num_seqs, staging, status, stream);
+}
+
+mla_status mla_cache_append_ex(const void* h, const void* w_dkv, const void* w_kr, const int32_t* seq_ids,
+                               const int32_t* pos, int T, int d_model, const mla_rope* rope, const mla_cache* cache,
+                               int num_seqs, void* staging, int32_t* status, cudaStream_t stream) {
   if (!h || !w_dkv || !w_kr || !seq_ids || !pos || !cache || !cache->data) return MLA_ERR_INVALID_ARG;
   if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(cache->data) || !aligned16(seq_ids) ||
       !aligned16(pos))
@@ -222,7 +251,8 @@ mla_status mla_cache_append(const void* h, const void* w_dkv, const void* w_kr, 
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_ERR_INVALID_ARG;
   if (T < 0 || T > kMaxBatch * 128) return MLA_ERR_INVALID_ARG;
   if (d_model < 512 || d_model > 32768 || d_model % 512) return d_model > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
-  if (!(rope_base > 1.f) || !std::isfinite(rope_base)) return MLA_ERR_INVALID_ARG;
+  RopeSpec spec;
+  if (!rope_spec(rope, &spec)) return MLA_ERR_INVALID_ARG;
   if (num_seqs < 1 || cache->reserved != 0 || cache->num_rows < 1) return MLA_ERR_INVALID_ARG;
   if (cache->dtype == MLA_KV_BF16) {
     if (cache->scales) return MLA_ERR_INVALID_ARG;
@@ -239,7 +269,7 @@ mla_status mla_cache_append(const void* h, const void* w_dkv, const void* w_kr, 
   }
   if (T == 0) return MLA_OK;
   return cuda_status(launch_cache_append(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(w_dkv),
-                                         static_cast<const __nv_bfloat16*>(w_kr), seq_ids, pos, T, d_model, rope_base,
+                                         static_cast<const __nv_bfloat16*>(w_kr), seq_ids, pos, T, d_model, spec,
                                          *cache, num_seqs, static_cast<__nv_bfloat16*>(staging), status, stream));
 }
 

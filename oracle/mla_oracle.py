@@ -55,20 +55,39 @@ def default_scale() -> float:
 # RoPE ([A] §"解耦 RoPE 与 YaRN": position is carried only by the 64-wide decoupled
 # query/key pair). Rotate-half pairing, written from the rotation definition.
 # ---------------------------------------------------------------------------------
-def rope(x, pos, base: float = ROPE_BASE) -> np.ndarray:
+def yarn_inv_freq(width: int, base: float, scale: float, alpha: float, beta: float, original_max_pos: int):
+    """Per-pair angular frequencies of RoPE extended by YaRN ([A] §"解耦 RoPE 与 YaRN":
+    YaRN on the decoupled key with scale 40, α = 1, β = 32; the pages give no formula,
+    so this is the published YaRN frequency rule): pair i's plain frequency θ_i turns
+    r_i = L_0 θ_i / (2π) times over the original context L_0; pairs that turn more than
+    β times keep θ_i, pairs that turn less than α times are slowed to θ_i / scale, and
+    in between the frequency moves linearly in r from one to the other."""
+    m = width // 2
+    i = np.arange(m, dtype=np.float64)
+    theta = base ** (-2.0 * i / width)
+    if scale == 1.0:
+        return theta
+    r = original_max_pos * theta / (2.0 * math.pi)
+    gamma = np.clip((r - alpha) / (beta - alpha), 0.0, 1.0)     # 0: fully slowed, 1: unchanged
+    return (1.0 - gamma) * theta / scale + gamma * theta
+
+
+def rope(x, pos, base: float = ROPE_BASE, inv_freq=None) -> np.ndarray:
     """Rotate the last axis of ``x`` (width 2m) by position ``pos``.
 
-    Element pair (i, i + m) is rotated by the angle pos · base^(-2i/(2m)):
-        x'_i     = x_i cos θ_i - x_{i+m} sin θ_i
-        x'_{i+m} = x_{i+m} cos θ_i + x_i sin θ_i
+    Element pair (i, i + m) is rotated by the angle pos · θ_i, θ_i = base^(-2i/(2m))
+    unless ``inv_freq`` (the m frequencies, e.g. from yarn_inv_freq) is given:
+        x'_i     = x_i cos(pos θ_i) - x_{i+m} sin(pos θ_i)
+        x'_{i+m} = x_{i+m} cos(pos θ_i) + x_i sin(pos θ_i)
     ``pos`` broadcasts against ``x.shape[:-1]``.
     """
     x = _f64(x)
     width = x.shape[-1]
     m = width // 2
-    i = np.arange(m, dtype=np.float64)
-    inv_freq = base ** (-2.0 * i / width)
-    theta = _f64(pos)[..., None] * inv_freq
+    if inv_freq is None:
+        i = np.arange(m, dtype=np.float64)
+        inv_freq = base ** (-2.0 * i / width)
+    theta = _f64(pos)[..., None] * _f64(inv_freq)
     c, s = np.cos(theta), np.sin(theta)
     x1, x2 = x[..., :m], x[..., m:]
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
@@ -78,7 +97,7 @@ def rope(x, pos, base: float = ROPE_BASE) -> np.ndarray:
 # Explicit form: up-project K and V per head, then plain softmax attention.
 # ---------------------------------------------------------------------------------
 def attend_explicit(q, c_kv, k_rope, w_uk, w_uv, pos_q, scale=None, heads=None,
-                    base: float = ROPE_BASE, return_p: bool = False):
+                    base: float = ROPE_BASE, return_p: bool = False, inv_freq=None):
     """Decode attention of one sequence, explicit (non-absorbed) form.
 
     q       [n_h, 192]  (q^C ‖ q^R before rotation)
@@ -99,7 +118,7 @@ def attend_explicit(q, c_kv, k_rope, w_uk, w_uv, pos_q, scale=None, heads=None,
     L = c.shape[0]
     scale = default_scale() if scale is None else float(scale)
     heads = range(n_h) if heads is None else heads
-    q_r = rope(q[:, D_H:], pos_q, base)
+    q_r = rope(q[:, D_H:], pos_q, base, inv_freq)
 
     o = np.zeros((n_h, D_H))
     o_lat = np.zeros((n_h, D_C))
@@ -191,7 +210,7 @@ def attend_latent(q_lat, rows, scale=None):
 # RoPE 与 YaRN": a shared 64-wide key carries the position, rotated where it is made;
 # hidden size 5120, [A] §"8.1T token 预训练配置与 H800 成本账" and [B] §"计算设置").
 # ---------------------------------------------------------------------------------
-def cache_rows(h, w_dkv, w_kr, pos, base: float = ROPE_BASE) -> np.ndarray:
+def cache_rows(h, w_dkv, w_kr, pos, base: float = ROPE_BASE, inv_freq=None) -> np.ndarray:
     """Cache rows of new tokens, unrounded.
 
     h      [T, d]     hidden states of the new tokens
@@ -203,7 +222,7 @@ def cache_rows(h, w_dkv, w_kr, pos, base: float = ROPE_BASE) -> np.ndarray:
     h = _f64(h)
     c = h @ _f64(w_dkv).T                                 # [T, 512]
     k_raw = h @ _f64(w_kr).T                              # [T, 64]
-    return np.concatenate([c, rope(k_raw, _f64(pos), base)], axis=-1)
+    return np.concatenate([c, rope(k_raw, _f64(pos), base, inv_freq)], axis=-1)
 
 
 # ---------------------------------------------------------------------------------

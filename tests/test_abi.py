@@ -210,3 +210,22 @@ def test_cache_append_rejects_bad_arguments_on_host():
     paged = dict(block_table=A, page_size=64, max_pages=64, num_rows=64 * 100)
     assert append(_cache(**{**paged, "page_size": 16})) == UNSUPPORTED
     assert append(_cache(**{**paged, "num_rows": 64 * 100 + 1})) == INVALID
+
+
+def test_rope_spec_is_checked_on_host():
+    L = _lib.get()
+
+    def absorb(**kw):
+        r = _lib.MlaRope()
+        r.base, r.yarn_scale, r.yarn_alpha, r.yarn_beta, r.original_max_pos, r.reserved = 10000.0, 40.0, 1.0, 32.0, 4096, 0
+        for k, v in kw.items():
+            setattr(r, k, v)
+        return L.mla_absorb_q_ex(A, A, A, 1, 128, ctypes.byref(r), None if kw.get("null_out") else A, None)
+
+    assert absorb(base=1.0) == INVALID
+    assert absorb(yarn_scale=0.5) == INVALID
+    assert absorb(yarn_beta=1.0) == INVALID          # beta must exceed alpha
+    assert absorb(yarn_alpha=-1.0) == INVALID
+    assert absorb(original_max_pos=0) == INVALID
+    assert absorb(reserved=1) == INVALID
+    assert L.mla_absorb_q_ex(A, A, A, 1, 128, None, A, None) == INVALID

@@ -311,3 +311,49 @@ def test_cache_rows_are_linear_in_the_hidden_state():
     lhs = M.cache_rows(2.5 * h - h2, w_dkv, w_kr, pos)
     rhs = 2.5 * M.cache_rows(h, w_dkv, w_kr, pos) - M.cache_rows(h2, w_dkv, w_kr, pos)
     np.testing.assert_allclose(lhs, rhs, rtol=1e-10, atol=1e-12)
+
+
+# ----------------------------- YaRN frequencies ------------------------------------
+YARN = dict(scale=40.0, alpha=1.0, beta=32.0, original_max_pos=4096)   # the pages' parameters, 4K pre-training
+
+
+def test_yarn_scale_one_is_plain_rope():
+    f = M.yarn_inv_freq(64, 10000.0, 1.0, 1.0, 32.0, 4096)
+    np.testing.assert_array_equal(f, 10000.0 ** (-np.arange(32) / 32.0))
+    x = np.random.default_rng(50).standard_normal((3, 64))
+    np.testing.assert_array_equal(M.rope(x, [1, 700, 90000], inv_freq=f), M.rope(x, [1, 700, 90000]))
+
+
+def test_yarn_bands_for_the_pages_parameters():
+    # Pair i turns r_i = 4096 · 10000^(-i/32) / (2π) times over the 4K context:
+    # r_10 = 36.7 and r_11 = 27.5 (β = 32 lies between), r_22 = 1.16 and r_23 = 0.87
+    # (α = 1 lies between). So pairs 0..10 keep their frequency, 23..31 are slowed by
+    # exactly 40, and 11..22 lie strictly in between.
+    plain = 10000.0 ** (-np.arange(32) / 32.0)
+    f = M.yarn_inv_freq(64, 10000.0, **YARN)
+    np.testing.assert_array_equal(f[:11], plain[:11])
+    np.testing.assert_allclose(f[23:], plain[23:] / 40.0, rtol=1e-15)
+    mid = f[11:23] / plain[11:23]
+    assert np.all((mid > 1 / 40.0) & (mid < 1.0))
+    assert np.all(np.diff(f / plain) <= 1e-15)   # the slowdown grows with the wavelength
+
+
+def test_yarn_frequency_of_a_ramp_pair():
+    # pair 16: θ = 0.01, r = 40.96 / (2π) = 6.51899, ramp (r - 1) / 31 = 0.178032,
+    # θ' = 0.01 · (0.178032 + 0.821968 / 40) = 0.00198581
+    f = M.yarn_inv_freq(64, 10000.0, **YARN)
+    assert f[16] == pytest.approx(0.0019858103, rel=1e-7)
+
+
+def test_yarn_keys_attend_by_relative_position():
+    rng = np.random.default_rng(51)
+    L, d = 5, 32
+    f = M.yarn_inv_freq(64, 10000.0, **YARN)
+    h, w_dkv, w_kr = _append_case(rng, T=L, d=d)
+    q, _, _, wk, wv = _rand_case(rng, n_h=2, L=L)
+    outs = []
+    for delta in (0, 3000, 150000):
+        rows = M.cache_rows(h, w_dkv, w_kr, np.arange(L) + delta, inv_freq=f)
+        outs.append(M.attend_explicit(q, rows[:, :512], rows[:, 512:], wk, wv, pos_q=L - 1 + delta, inv_freq=f))
+    for o in outs[1:]:
+        np.testing.assert_allclose(o["o"], outs[0]["o"], rtol=1e-9, atol=1e-12)

@@ -57,7 +57,7 @@ ORACLE_MUTANTS = [
     ("attend_explicit", "wk = _f64(w_uk[h])", "wk = _f64(w_uv[h])"),
     ("attend_explicit", "V = c @ wv.T", "V = c @ wk.T"),
     ("attend_explicit", "K = np.concatenate([c @ wk.T, kr], axis=1)", "K = np.concatenate([c @ wk.T, 0.0 * kr], axis=1)"),
-    ("attend_explicit", "q_r = rope(q[:, D_H:], pos_q, base)", "q_r = rope(q[:, D_H:], pos_q + 1, base)"),
+    ("attend_explicit", "q_r = rope(q[:, D_H:], pos_q, base, inv_freq)", "q_r = rope(q[:, D_H:], pos_q + 1, base, inv_freq)"),
     ("attend_explicit", "s = (K @ qh) * scale", "s = K @ qh"),
     ("attend_explicit", "p = e / z", "p = e / e.max()"),
     ("attend_explicit", "o_lat[h] = p @ c", "o_lat[h] = e @ c"),
@@ -79,9 +79,14 @@ ORACLE_MUTANTS = [
     ("mha_cache_elements", "return 2 * n_h * d_h * layers", "return n_h * d_h * layers"),
     # writing the cache: which weight, the key's rotation and its position
     ("cache_rows", "c = h @ _f64(w_dkv).T", "c = h @ _f64(w_dkv).T * 1.0001"),
-    ("cache_rows", "rope(k_raw, _f64(pos), base)", "rope(k_raw, -_f64(pos), base)"),
-    ("cache_rows", "rope(k_raw, _f64(pos), base)", "rope(k_raw, _f64(pos) + 1, base)"),
-    ("cache_rows", "rope(k_raw, _f64(pos), base)", "k_raw"),
+    ("cache_rows", "rope(k_raw, _f64(pos), base, inv_freq)", "rope(k_raw, -_f64(pos), base, inv_freq)"),
+    ("cache_rows", "rope(k_raw, _f64(pos), base, inv_freq)", "rope(k_raw, _f64(pos) + 1, base, inv_freq)"),
+    ("cache_rows", "rope(k_raw, _f64(pos), base, inv_freq)", "k_raw"),
+    # YaRN: the ramp's direction, its end points, the slowed frequency
+    ("yarn_inv_freq", "return (1.0 - gamma) * theta / scale + gamma * theta", "return gamma * theta / scale + (1.0 - gamma) * theta"),
+    ("yarn_inv_freq", "gamma = np.clip((r - alpha) / (beta - alpha), 0.0, 1.0)", "gamma = np.clip((r - alpha) / beta, 0.0, 1.0)"),
+    ("yarn_inv_freq", "r = original_max_pos * theta / (2.0 * math.pi)", "r = original_max_pos * theta"),
+    ("yarn_inv_freq", "return (1.0 - gamma) * theta / scale + gamma * theta", "return (1.0 - gamma) * theta * scale + gamma * theta"),
     ("cache_rows", "k_raw = h @ _f64(w_kr).T", "k_raw = h @ _f64(w_dkv[:64]).T"),
 ]
 
