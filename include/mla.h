@@ -236,6 +236,30 @@ MLA_API mla_status mla_cache_append_ex(const void* h, const void* w_dkv, const v
                                        int32_t* status, cudaStream_t stream);
 
 /*
+ * mla_multi_token_view — several new query tokens per sequence (speculative or chunked
+ * decoding), decoded as B*T sequences of one paged view of the same cache.
+ *   ("DeepSeek-V2 机制拆解", §"长上下文推理的第一瓶颈": every new token attends to all
+ *    earlier tokens; with T new tokens at the end of sequence b, query j sits at
+ *    position L_b - T + j and sees tokens 0 .. L_b - T + j.)
+ *   Sequence v = b*T + j of the view: view_seq_lens[v] = max(L_b - T + j + 1, 0),
+ *   view_pos[v] = max(view_seq_lens[v] - 1, 0) (the query position for mla_absorb_q),
+ *   block-table row v = the pages of sequence b (a paged cache's own row, or for a
+ *   contiguous cache its rows b*seq_stride .. taken 64 at a time, which needs
+ *   seq_stride_tokens and num_rows to be multiples of 64, else MLA_ERR_UNSUPPORTED).
+ *   `*view` (host) receives the paged view: the same rows and scales, this block table.
+ *   The step is then mla_absorb_q (B*T queries, view_pos), mla_decode_fwd over `view`
+ *   with view_seq_lens, mla_combine and mla_up_v, all on B*T sequences.
+ *   seq_lens [B] int32 device; view_seq_lens, view_pos [B*T] int32 device out;
+ *   view_block_table [B*T, view_max_pages] int32 device out, view_max_pages >=
+ *   ceil(max_seq_len / 64). B*T <= 65535.
+ */
+MLA_API mla_status mla_multi_token_view(const mla_cache* cache, const int32_t* seq_lens, int B,
+                                        int T, int max_seq_len, int32_t* view_seq_lens,
+                                        int32_t* view_pos, int32_t* view_block_table,
+                                        int view_max_pages, mla_cache* view,
+                                        cudaStream_t stream);
+
+/*
  * mla_quantize_fp8 — cache-write helper: bf16 rows → e4m3 rows + per-row scale.
  *   The pages report a low-bit KV cache for serving ("DeepSeek-V2 机制拆解",
  *   §"推理参数与 128K 上下文的使用注意"; "中文验证版", §"方法适配") without its format;

@@ -27,7 +27,8 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_MAX_SPLITS, MlaCache, MlaEr
                    status_string)
 
 __all__ = [
-    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "cache_append", "num_splits", "split_range",
+    "absorb_q", "decode_fwd", "combine", "up_v", "quantize_fp8", "cache_append", "decode_multi", "num_splits",
+    "split_range",
     "decode_kernel",
     "decode_combine_static",
     "compute_dtype",
@@ -390,6 +391,38 @@ def decode_step(q, w_uk, w_uv, cache: Cache, seq_lens, pos, max_seq_len: int, n_
     o_lat, lse = combine(o_part, lse_part, o_lat=bufs.get("o_lat"), lse=bufs.get("lse"), stream=stream)
     o = up_v(o_lat, w_uv, o=bufs.get("o"), stream=stream)
     return dict(q_lat=q_lat, o_part=o_part, lse_part=lse_part, o_lat=o_lat, lse=lse, o=o)
+
+
+def decode_multi(q, w_uk, w_uv, cache: Cache, seq_lens, max_seq_len: int, n_splits: int = 0,
+                 softmax_scale: float | None = None, rope_base: float = 10000.0, status=None, stream=None,
+                 yarn: Yarn | None = None):
+    """T new query tokens per sequence (include/mla.h, mla_multi_token_view): the last T
+    cached tokens of sequence b are its new ones, query j sits at position L_b - T + j and
+    sees tokens 0 .. L_b - T + j. q [B, T, n_h, 192] bf16 → dict of the step's outputs
+    with o [B, T, n_h, 128]. The library builds a paged view of the cache with one
+    sequence per query and runs the four calls on it."""
+    B, T, n_h = q.shape[0], q.shape[1], q.shape[2]
+    _need(q, "q", torch.bfloat16, (B, T, n_h, D_Q))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    mp = max((int(max_seq_len) + PAGE - 1) // PAGE, 1)
+    dev_t = q.device
+    v_lens = torch.empty(B * T, dtype=torch.int32, device=dev_t)
+    v_pos = torch.empty(B * T, dtype=torch.int32, device=dev_t)
+    v_table = torch.empty(B * T, mp, dtype=torch.int32, device=dev_t)
+    c = cache.to_c()
+    view = MlaCache()
+    dev = _one_device(q=q, seq_lens=seq_lens, **cache.tensors())
+    _call("mla_multi_token_view", dev, ctypes.byref(c), _ptr(seq_lens), B, T, int(max_seq_len), _ptr(v_lens),
+          _ptr(v_pos), _ptr(v_table), mp, ctypes.byref(view), stream=stream)
+    # the same rows as 64-row pages (the view's block table indexes them)
+    pages = cache.data.shape[0] * cache.data.shape[1] // PAGE
+    v_cache = Cache(cache.data.view(pages, PAGE, D_ROW),
+                    None if cache.scales is None else cache.scales.view(pages, PAGE), v_table)
+    out = decode_step(q.view(B * T, n_h, D_Q), w_uk, w_uv, v_cache, v_lens, v_pos, max_seq_len, n_splits=n_splits,
+                      softmax_scale=softmax_scale, rope_base=rope_base, status=status, stream=stream, yarn=yarn)
+    out["o"] = out["o"].view(B, T, n_h, D_NOPE)
+    out["view_seq_lens"], out["view_pos"] = v_lens, v_pos
+    return out
 
 
 class DecodeStepGraph:

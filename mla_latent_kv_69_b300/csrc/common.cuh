@@ -98,6 +98,9 @@ cudaError_t launch_cache_append(const __nv_bfloat16* h, const __nv_bfloat16* w_d
                                 const int32_t* seq_ids, const int32_t* pos, int T, int d, const RopeSpec& rope,
                                 const mla_cache& cache, int num_seqs, __nv_bfloat16* staging, int32_t* status,
                                 cudaStream_t st);
+cudaError_t launch_multi_token_view(const int32_t* seq_lens, int B, int T, const mla_cache& cache,
+                                    int max_pages_out, int32_t* out_lens, int32_t* out_pos, int32_t* out_table,
+                                    cudaStream_t st);
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t n, uint8_t* codes, float* scales,
                                 cudaStream_t st);
 

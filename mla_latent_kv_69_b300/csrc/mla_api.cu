@@ -273,6 +273,33 @@ mla_status mla_cache_append_ex(const void* h, const void* w_dkv, const void* w_k
                                          *cache, num_seqs, static_cast<__nv_bfloat16*>(staging), status, stream));
 }
 
+mla_status mla_multi_token_view(const mla_cache* cache, const int32_t* seq_lens, int B, int T, int max_seq_len,
+                                int32_t* view_seq_lens, int32_t* view_pos, int32_t* view_block_table,
+                                int view_max_pages, mla_cache* view, cudaStream_t stream) {
+  if (!cache || !cache->data || !seq_lens || !view_seq_lens || !view_pos || !view_block_table || !view)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(seq_lens) || !aligned16(view_seq_lens) || !aligned16(view_pos) || !aligned16(view_block_table))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || T < 1 || (int64_t)B * T > kMaxBatch || max_seq_len < 0) return MLA_ERR_INVALID_ARG;
+  if (view_max_pages < ceil_div(max_seq_len, kPage) || view_max_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (cache->reserved != 0 || cache->num_rows < 1) return MLA_ERR_INVALID_ARG;
+  if (cache->block_table) {
+    if (cache->page_size != kPage) return cache->page_size > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+    if (!aligned16(cache->block_table) || cache->max_pages < 1) return MLA_ERR_INVALID_ARG;
+  } else {
+    // the view pages a contiguous cache in place: whole 64-row pages per sequence
+    if (cache->seq_stride_tokens < max_seq_len || cache->seq_stride_tokens < 1) return MLA_ERR_INVALID_ARG;
+    if (cache->seq_stride_tokens % kPage || cache->num_rows % kPage) return MLA_ERR_UNSUPPORTED;
+  }
+  *view = *cache;
+  view->block_table = view_block_table;
+  view->page_size = kPage;
+  view->max_pages = view_max_pages;
+  view->seq_stride_tokens = 0;
+  return cuda_status(launch_multi_token_view(seq_lens, B, T, *cache, view_max_pages, view_seq_lens, view_pos,
+                                             view_block_table, stream));
+}
+
 mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t* codes, float* scales,
                             cudaStream_t stream) {
   if (!rows || !codes || !scales) return MLA_ERR_INVALID_ARG;

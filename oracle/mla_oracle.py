@@ -205,6 +205,30 @@ def attend_latent(q_lat, rows, scale=None):
 
 
 # ---------------------------------------------------------------------------------
+# Several new query tokens per sequence (speculative or chunked decoding). The pages
+# describe decoding as each new token attending to every earlier token ([A] §"长上下文推理
+# 的第一瓶颈"); with T new tokens cached at the end of a sequence of L tokens, query j
+# (0 <= j < T) sits at position L - T + j and attends causally to tokens 0 .. L - T + j.
+# ---------------------------------------------------------------------------------
+def attend_multi(q, c_kv, k_rope, w_uk, w_uv, T: int, scale=None, base: float = ROPE_BASE, inv_freq=None):
+    """q [T, n_h, 192]; c_kv [L, 512], k_rope [L, 64] (the last T rows are the new
+    tokens). Returns dict with o [T, n_h, 128], lse [T, n_h], o_lat [T, n_h, 512]; a
+    query with no visible token (L - T + j < 0) gets o = o_lat = 0 and lse = -inf."""
+    q = _f64(q)
+    L = np.asarray(c_kv).shape[0]
+    n_h = q.shape[1]
+    outs = []
+    for j in range(T):
+        p = L - T + j
+        if p < 0:
+            outs.append(dict(o=np.zeros((n_h, D_H)), lse=np.full(n_h, -np.inf), o_lat=np.zeros((n_h, D_C))))
+            continue
+        outs.append(attend_explicit(q[j], c_kv[:p + 1], k_rope[:p + 1], w_uk, w_uv, pos_q=p, scale=scale, base=base,
+                                    inv_freq=inv_freq))
+    return {k: np.stack([o[k] for o in outs]) for k in ("o", "lse", "o_lat")}
+
+
+# ---------------------------------------------------------------------------------
 # Writing the cache ([A] §"长上下文推理的第一瓶颈": each token's hidden state is
 # down-projected to the latent c_KV, d_c = 512, and only that is cached; [A] §"解耦
 # RoPE 与 YaRN": a shared 64-wide key carries the position, rotated where it is made;

@@ -229,3 +229,19 @@ def test_rope_spec_is_checked_on_host():
     assert absorb(original_max_pos=0) == INVALID
     assert absorb(reserved=1) == INVALID
     assert L.mla_absorb_q_ex(A, A, A, 1, 128, None, A, None) == INVALID
+
+
+def test_multi_token_view_rejects_bad_arguments_on_host():
+    L = _lib.get()
+
+    def view(c=None, B=4, T=2, max_len=4096, mp=64, out=A):
+        c = _cache() if c is None else c
+        v = _lib.MlaCache()
+        return L.mla_multi_token_view(ctypes.byref(c), A, B, T, max_len, out, A, A, mp, ctypes.byref(v), None)
+
+    assert view(T=0) == INVALID
+    assert view(B=40000, T=2) == INVALID                          # B*T beyond the grid limit
+    assert view(mp=10) == INVALID                                 # too few pages for max_seq_len
+    assert view(out=MIS) == INVALID
+    assert view(_cache(seq_stride_tokens=4100, num_rows=32 * 4100)) == UNSUPPORTED   # not whole pages
+    assert view(max_len=5000) == INVALID                          # longer than the contiguous stride

@@ -357,3 +357,49 @@ def test_yarn_keys_attend_by_relative_position():
         outs.append(M.attend_explicit(q, rows[:, :512], rows[:, 512:], wk, wv, pos_q=L - 1 + delta, inv_freq=f))
     for o in outs[1:]:
         np.testing.assert_allclose(o["o"], outs[0]["o"], rtol=1e-9, atol=1e-12)
+
+
+# ------------------------------ several new tokens ---------------------------------
+def _multi_case(rng, T=3, L=9, n_h=2):
+    _, c, kr, wk, wv = _rand_case(rng, n_h=n_h, L=L)
+    q = rng.standard_normal((T, n_h, 192))
+    return q, c, kr, wk, wv
+
+
+def test_multi_token_last_query_is_the_single_token_decode():
+    rng = np.random.default_rng(60)
+    q, c, kr, wk, wv = _multi_case(rng)
+    out = M.attend_multi(q, c, kr, wk, wv, T=3)
+    single = M.attend_explicit(q[2], c, kr, wk, wv, pos_q=c.shape[0] - 1)
+    np.testing.assert_allclose(out["o"][2], single["o"], rtol=1e-12, atol=1e-14)
+    one = M.attend_multi(q[2:], c, kr, wk, wv, T=1)
+    np.testing.assert_allclose(one["o"][0], single["o"], rtol=1e-12, atol=1e-14)
+
+
+def test_multi_token_queries_do_not_see_later_tokens():
+    # query j sees tokens 0 .. L - T + j: changing the tokens after that position changes
+    # nothing for it, and changing the token at that position does
+    rng = np.random.default_rng(61)
+    q, c, kr, wk, wv = _multi_case(rng, T=4, L=10)
+    base = M.attend_multi(q, c, kr, wk, wv, T=4)
+    for j in range(4):
+        p = 10 - 4 + j
+        c2, kr2 = c.copy(), kr.copy()
+        c2[p + 1:] += 5.0
+        kr2[p + 1:] -= 3.0
+        out = M.attend_multi(q, c2, kr2, wk, wv, T=4)
+        np.testing.assert_array_equal(out["o"][j], base["o"][j])
+        c3 = c.copy()
+        c3[p] += 1.0
+        assert not np.allclose(M.attend_multi(q, c3, kr, wk, wv, T=4)["o"][j], base["o"][j])
+
+
+def test_multi_token_positions_and_empty_queries():
+    # with L < T the first T - L queries see no token; the others sit at 0, 1, ...
+    rng = np.random.default_rng(62)
+    q, c, kr, wk, wv = _multi_case(rng, T=4, L=2)
+    out = M.attend_multi(q, c, kr, wk, wv, T=4)
+    assert np.all(out["o"][:2] == 0) and np.all(np.isneginf(out["lse"][:2]))
+    # query 2 sees token 0 alone: its output is that token's value, W_UV · c_0
+    np.testing.assert_allclose(out["o"][2], np.einsum("hdj,j->hd", wv, c[0]), rtol=1e-12)
+    np.testing.assert_allclose(out["o_lat"][2], np.broadcast_to(c[0], (2, 512)), rtol=1e-12)

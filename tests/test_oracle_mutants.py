@@ -88,6 +88,11 @@ ORACLE_MUTANTS = [
     ("yarn_inv_freq", "r = original_max_pos * theta / (2.0 * math.pi)", "r = original_max_pos * theta"),
     ("yarn_inv_freq", "return (1.0 - gamma) * theta / scale + gamma * theta", "return (1.0 - gamma) * theta * scale + gamma * theta"),
     ("cache_rows", "k_raw = h @ _f64(w_kr).T", "k_raw = h @ _f64(w_dkv[:64]).T"),
+    # several new tokens: the query position, what it sees
+    ("attend_multi", "p = L - T + j", "p = L - T + j - 1"),
+    ("attend_multi", "outs.append(attend_explicit(q[j], c_kv[:p + 1], k_rope[:p + 1], w_uk, w_uv, pos_q=p,",
+     "outs.append(attend_explicit(q[j], c_kv, k_rope, w_uk, w_uv, pos_q=p,"),
+    ("attend_multi", "if p < 0:", "if p <= 0:"),
 ]
 
 
