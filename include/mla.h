@@ -295,9 +295,9 @@ MLA_API mla_status mla_decode_combine_static(const void* q_lat, const mla_cache*
 
 /* Decode kernels (mla_decode_kernel's answer). */
 #define MLA_KERNEL_TC_BF16 1    /* tcgen05 tensor-core kernel, bf16 operands, fp32 accum.*/
-#define MLA_KERNEL_TC_F16_E4M3 2 /* tcgen05 kernel for an e4m3 cache: codes converted to f16
-                                   exactly (as 2^-8 x value), query converted to f16,
-                                   fp32 accumulation                                     */
+#define MLA_KERNEL_TC_E4M3 2     /* tcgen05 kernel for an e4m3 cache: QK^T on the codes
+                                    (kind::f8f6f4, the query as two e4m3 parts), PV on f16
+                                    operands converted from the codes; fp32 accumulation */
 
 /* Which decode kernel mla_decode_fwd runs for this cache dtype and head count
  * (-1 for an invalid combination). Host only. */

@@ -197,12 +197,12 @@ class Cache:
 def decode_kernel(kv: str, n_h: int) -> str:
     """Name of the decode kernel the library runs for a cache dtype ("bf16"/"fp8") and head count."""
     code = int(_lib.get().mla_decode_kernel(MLA_KV_FP8_E4M3 if kv == "fp8" else MLA_KV_BF16, n_h))
-    return {1: "tcgen05_bf16", 2: "tcgen05_f16_e4m3"}.get(code, "invalid")
+    return {1: "tcgen05_bf16", 2: "tcgen05_e4m3"}.get(code, "invalid")
 
 
 def compute_dtype(n_h: int, kv: str) -> str:
     """Arithmetic type of the decode kernel's contractions."""
-    return {"tcgen05_bf16": "bf16", "tcgen05_f16_e4m3": "f16"}.get(decode_kernel(kv, n_h), "?")
+    return {"tcgen05_bf16": "bf16", "tcgen05_e4m3": "e4m3/f16"}.get(decode_kernel(kv, n_h), "?")
 
 
 def num_splits(B: int, max_seq_len: int, n_h: int) -> int:

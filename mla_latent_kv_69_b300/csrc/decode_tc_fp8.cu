@@ -6,19 +6,22 @@
 // cluster of two CTAs per (sequence, split); the score CTA holds Q and S in TMEM and
 // runs the softmax, the value CTA holds the 128 x 512 fp32 O accumulator.
 //
-// A kind::f16 MMA takes two operands of one type and an 8-bit query would not keep the
-// error budget, so both contractions run on f16 operands: every e4m3 code maps to the f16
-// of 2^-8 times its value, which is exact (see e4m3x16_to_f16), and each head's query is
-// multiplied by a power of two 2^k_h that puts its largest element in [2^14, 2^15) before
-// it converts from bf16 to f16 (11 significant bits against bf16's 8), so no query
-// overflows f16 or loses its significant elements to f16's subnormal range.
-// The 2^8 and 2^-k_h come back in fp32, in the score scale and in the output's 1/l.
-// Each CTA has four converter warps that
-// turn TMA-loaded e4m3 rows into 128B-swizzled f16 operand tiles:
-//   score CTA  e4m3 ring of five 24 KB groups (128 tokens x 3 column chunks) →
-//              four 16 KB f16 slots (128 tokens x 64 columns) → 4 MMAs each;
+// S = Q · code^T runs straight on the TMA-loaded codes (tcgen05 kind::f8f6f4, both
+// operands e4m3): each head's query is multiplied by a power of two 2^k_h that puts its
+// largest element in [2^7, 2^8) and split into two e4m3 parts, hi = e4m3(q) and
+// lo = e4m3(q - hi), whose sum is the bf16 value exactly for every element within 2^-16
+// of the head's largest (a bf16 value has 8 significant bits, e4m3 4); the two parts are
+// two MMAs of K = 32 per step, which cost one f16 MMA of K = 16, so QK^T takes the bf16
+// kernel's tensor time with no conversion of the cache. The score side loads its codes as
+// 64B-swizzled [128 tokens][64 codes] chunks (the MMA's K-major operand layout).
+// O += P' · V keeps f16 operands (an 8-bit P would not keep the error budget): every
+// e4m3 code maps to the f16 of 2^-8 times its value, which is exact (see
+// e4m3x16_to_f16); the value CTA's four converter warps turn its TMA-loaded e4m3 rows
+// into 128B-swizzled f16 tiles:
 //   value CTA  e4m3 ring of two 32 KB steps (64 tokens x 512 columns) → two 64 KB f16
 //              stages → 8 MMAs of N = 256 per step (rows past the split are zeroed).
+// The score CTA's four extra warps only stage each tile's per-token scales. 2^-k_h
+// comes back in fp32 in the score scale, the value side's 2^8 in the output's 1/l.
 // The per-token scale stays outside the MMAs. The score CTA multiplies each score column
 // by it (x_t = scale_t · Q·code_t, log2 units) and runs the online softmax on the log2
 // weight of the codes, y_t = x_t + log2 scale_t: the value CTA receives P'_t = 2^(y_t - m)
@@ -49,10 +52,9 @@ constexpr int kConvBase = 320;             // first converter thread
 constexpr uint64_t kWaitNs = kDecodeWaitNs;
 constexpr float kRescaleLog2 = 8.f;
 
-constexpr int kE4Group = 2 * 3 * 64 * 64;  // score e4m3 group: [2 halves][3 chunks][64 rows][64 B]
-constexpr int kE4Ring = 5;
-constexpr int kF16Slot = 128 * 128;        // score f16 slot: 128 rows x 64 columns, 128B swizzle
-constexpr int kF16Ring = 4;
+constexpr int kE4Chunk = 128 * 64;        // score operand chunk: 128 tokens x 64 codes, 64B swizzle (8 KB)
+constexpr int kE4Group = 3 * kE4Chunk;     // score e4m3 group: three chunks (24 KB)
+constexpr int kE4Ring = 7;
 constexpr int kVE4 = 8 * 64 * 64;          // value e4m3 step: [8 chunks][64 rows][64 B]
 constexpr int kVStage = 8 * 64 * 128;      // value f16 stage: [8 chunks][64 rows][128 B], 128B swizzle
 constexpr int kPanel = 128 * 128;          // P for 64 tokens: 128 heads x 64 f16
@@ -60,14 +62,14 @@ constexpr int kHdr = 512 + 16;
 constexpr int kFinBytes = 128 * 2 * 4;
 constexpr int kQGroup = 3 * 128 * 128;     // Q staging: three chunk groups of up to 128 rows (bf16)
 
-constexpr uint32_t kQCol = 0;              // score CTA TMEM: Q as f16 pairs (288 columns)
+constexpr uint32_t kQCol = 0;              // score CTA TMEM: Q as e4m3, high parts (144 columns, 4 per column)
+constexpr uint32_t kQLoCol = 144;          // score CTA TMEM: Q as e4m3, low parts (144 columns)
 constexpr uint32_t kSCol = 288;            // score CTA TMEM: S (128 columns)
 constexpr uint32_t kOCol = 0;              // value CTA TMEM: O (512 columns)
 
 //   score CTA
 constexpr int S_E4 = 0;
-constexpr int S_F16 = S_E4 + kE4Ring * kE4Group;
-constexpr int S_PANEL = S_F16 + kF16Ring * kF16Slot;
+constexpr int S_PANEL = S_E4 + kE4Ring * kE4Group;
 constexpr int S_HDR = S_PANEL + 2 * kPanel;
 constexpr int S_MX = S_HDR + 1024;
 constexpr int kSclBuf = 3 * 128;           // per tile: scale_t, log2 scale_t, 1 / scale_t (fp32)
@@ -82,10 +84,8 @@ constexpr int V_END = V_HDR + 1024;
 constexpr int OFF_BAR = (S_END > V_END ? S_END : V_END);
 enum Bar {
   SB_E4FULL = 0,                          // [kE4Ring] e4m3 group landed
-  SB_E4EMPTY = SB_E4FULL + kE4Ring,       // [kE4Ring] converters done with it (4 warps)
-  SB_F16FULL = SB_E4EMPTY + kE4Ring,      // [kF16Ring] f16 slot written (4 warps)
-  SB_F16EMPTY = SB_F16FULL + kF16Ring,    // [kF16Ring] QK MMAs done with it
-  SB_QFULL = SB_F16EMPTY + kF16Ring,
+  SB_E4EMPTY = SB_E4FULL + kE4Ring,       // [kE4Ring] QK MMAs done with it
+  SB_QFULL = SB_E4EMPTY + kE4Ring,
   SB_QREADY = SB_QFULL + 1,               // (256)
   SB_SFULL = SB_QREADY + 1,
   SB_SFREE = SB_SFULL + 1,                // (256)
@@ -108,7 +108,7 @@ enum Bar {
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
 constexpr int kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(S_F16 % 1024 == 0 && S_PANEL % 1024 == 0 && V_F16 % 1024 == 0 && V_PANEL % 1024 == 0,
+static_assert(kE4Group % 1024 == 0 && S_PANEL % 1024 == 0 && V_F16 % 1024 == 0 && V_PANEL % 1024 == 0,
               "swizzle alignment");
 static_assert(3 * kQGroup <= S_PANEL, "Q staging fits below the panels");
 
@@ -205,11 +205,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
     *o_init_word = 0;
     for (int k = 0; k < kE4Ring; ++k) {
       mbar_init(&bars[SB_E4FULL + k], 1);
-      mbar_init(&bars[SB_E4EMPTY + k], 4);
-    }
-    for (int k = 0; k < kF16Ring; ++k) {
-      mbar_init(&bars[SB_F16FULL + k], 4);
-      mbar_init(&bars[SB_F16EMPTY + k], 1);
+      mbar_init(&bars[SB_E4EMPTY + k], 1);
     }
     mbar_init(&bars[SB_QFULL], 1);
     mbar_init(&bars[SB_QREADY], 256);
@@ -252,7 +248,9 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
     // =============================== score CTA =========================================
     if (warp == 0) {
       if (lane == 0) {
-        // ---- TMA producer: Q (bf16), then e4m3 groups of 128 tokens x 3 chunks ----
+        // ---- TMA producer: Q (bf16), then e4m3 groups of 128 tokens x 3 chunks, each
+        // chunk a 64B-swizzled [128 tokens][64 codes] block: one box for a contiguous
+        // cache, one per page and chunk (64 rows) for a paged one ----
         const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_norm = l2_policy_evict_normal();   // the value CTA reads the rows again
         prefetch_tmap(&e4s_map);
@@ -266,6 +264,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         int issued = 0;
         if (!mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs)) give_up(p, abort_flag, smem, peer);
         HalfInfo h0{}, h1{};
+        const bool paged = p.block_table != nullptr;
         for (int k = 0; k < 3 * n_tiles && !*abort_flag; ++k) {
           const int i = k / 3, g = k % 3, e = k % kE4Ring;
           if (k >= kE4Ring &&
@@ -278,13 +277,26 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
             h1 = half_info(p, b, st, en, 2 * i + 1, true);
           }
           unsigned char* dst = smem + S_E4 + e * kE4Group;
-          const uint32_t bytes = (h0.load ? kE4Group / 2 : 0) + (h1.load ? kE4Group / 2 : 0);
-          if (bytes) {
-            mbar_arrive_expect_tx(&bars[SB_E4FULL + e], bytes);
-            if (h0.load) tma_load_3d(dst, &e4s_map, &bars[SB_E4FULL + e], 0, h0.row0, 3 * g, pol_norm);
-            if (h1.load) tma_load_3d(dst + kE4Group / 2, &e4s_map, &bars[SB_E4FULL + e], 0, h1.row0, 3 * g, pol_norm);
-          } else {
-            mbar_arrive(&bars[SB_E4FULL + e]);
+          if (!paged) {   // 128 consecutive rows (those past the split are masked)
+            if (h0.load) {
+              mbar_arrive_expect_tx(&bars[SB_E4FULL + e], kE4Group);
+              tma_load_3d(dst, &e4s_map, &bars[SB_E4FULL + e], 0, h0.row0, 3 * g, pol_norm);
+            } else {
+              mbar_arrive(&bars[SB_E4FULL + e]);
+            }
+          } else {        // page 0 → rows 0..63 of each chunk, page 1 → rows 64..127
+            const uint32_t bytes = 3 * ((h0.load ? kE4Chunk / 2 : 0) + (h1.load ? kE4Chunk / 2 : 0));
+            if (bytes) {
+              mbar_arrive_expect_tx(&bars[SB_E4FULL + e], bytes);
+              for (int c = 0; c < 3; ++c) {
+                if (h0.load) tma_load_3d(dst + c * kE4Chunk, &e4s_map, &bars[SB_E4FULL + e], 0, h0.row0, 3 * g + c, pol_norm);
+                if (h1.load)
+                  tma_load_3d(dst + c * kE4Chunk + kE4Chunk / 2, &e4s_map, &bars[SB_E4FULL + e], 0, h1.row0, 3 * g + c,
+                              pol_norm);
+              }
+            } else {
+              mbar_arrive(&bars[SB_E4FULL + e]);
+            }
           }
           issued = k + 1;
         }
@@ -295,8 +307,9 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        // ---- S = Q · code^T on f16 operands, 36 MMAs of 128 x 128 x 16 per tile ----
-        const uint32_t idq = idesc_f16(128, kTile, /*fp16_inputs=*/true, false, false);
+        // ---- S = (Q_hi + Q_lo) · code^T straight on the e4m3 codes: per 32-code step
+        // two kind::f8f6f4 MMAs of 128 x 128 x 32, 36 per tile ----
+        const uint32_t idq = idesc_e4m3(128, kTile);
         bool ok = mbar_wait(&bars[SB_QREADY], 0, abort_flag, kWaitNs);
         if (ok) mbar_arrive_remote(&bars[VB_GO], 1);
         for (int i = 0; ok && i < n_tiles; ++i) {
@@ -304,19 +317,25 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
             ok = false;
             break;
           }
-          for (int c = 0; c < 9; ++c) {
-            const int fi = 9 * i + c, f = fi % kF16Ring;
-            if (!mbar_wait(&bars[SB_F16FULL + f], (fi / kF16Ring) & 1, abort_flag, kWaitNs)) {
+          for (int g = 0; g < 3; ++g) {
+            const int k = 3 * i + g, e = k % kE4Ring;
+            if (!mbar_wait(&bars[SB_E4FULL + e], (k / kE4Ring) & 1, abort_flag, kWaitNs)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t base = smem_u32(smem + S_F16 + f * kF16Slot);
+            const uint32_t base = smem_u32(smem + S_E4 + e * kE4Group);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kSCol, tmem + kQCol + 8 * (4 * c + kk), sdesc_sw128(base + 32 * kk, 16, 1024), idq,
-                     (c | kk) ? 1u : 0u);
-            mma_commit(&bars[SB_F16EMPTY + f]);
+            for (int c = 0; c < 3; ++c)
+#pragma unroll
+              for (int ks = 0; ks < 2; ++ks) {
+                // codes 64 (3 g + c) + 32 ks .. + 31: TMEM column (that index) / 4
+                const uint32_t col = 16 * (3 * g + c) + 8 * ks;
+                const uint64_t bd = sdesc_sw64(base + c * kE4Chunk + 32 * ks, 512);
+                mma_ts_f8(tmem + kSCol, tmem + kQCol + col, bd, idq, (g | c | ks) ? 1u : 0u);
+                mma_ts_f8(tmem + kSCol, tmem + kQLoCol + col, bd, idq, 1u);
+              }
+            mma_commit(&bars[SB_E4EMPTY + e]);
           }
           if (!ok) break;
           mma_commit(&bars[SB_SFULL]);
@@ -327,7 +346,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         mbar_wait(&bars[SB_FLUSH], 0, &never, kWaitNs);
       }
     } else if (warp >= 10) {
-      // ---- converters: tile scales, then e4m3 → f16 slots, one row per thread ----
+      // ---- scale warps: each tile's per-token scales (the MMAs read the codes as they
+      // are), one row per thread ----
       const int ct = threadIdx.x - kConvBase;
       const int r = ct, hh = r >> 6, rr = r & 63;
       float* scl = reinterpret_cast<float*>(smem + S_SCL);
@@ -345,44 +365,15 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
           ok = false;
           break;
         }
-        {
-          // rows past the split (scale 0) get log2 = -inf and 1/scale = 0; their scores
-          // are masked to -inf anyway
-          float* sb = scl + (i & 1) * kSclBuf;
-          const bool pos = sc_next > 0.f;
-          sb[r] = sc_next;
-          sb[128 + r] = pos ? __log2f(sc_next) : -INFINITY;
-          sb[256 + r] = pos ? __frcp_rn(sc_next) : 0.f;
-        }
+        // rows past the split (scale 0) get log2 = -inf and 1/scale = 0; their scores
+        // are masked to -inf anyway
+        float* sb = scl + (i & 1) * kSclBuf;
+        const bool pos = sc_next > 0.f;
+        sb[r] = sc_next;
+        sb[128 + r] = pos ? __log2f(sc_next) : -INFINITY;
+        sb[256 + r] = pos ? __frcp_rn(sc_next) : 0.f;
         mbar_arrive(&bars[SB_SCLREADY + (i & 1)]);
         sc_next = row_scale(i + 1);
-        for (int c = 0; c < 9; ++c) {
-          const int k = 3 * i + c / 3, e = k % kE4Ring;
-          const int fi = 9 * i + c, f = fi % kF16Ring;
-          if (c % 3 == 0 && !warp_wait(&bars[SB_E4FULL + e], (k / kE4Ring) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (fi >= kF16Ring && !warp_wait(&bars[SB_F16EMPTY + f], ((fi / kF16Ring) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          // 128 rows x 64 codes: unit u = 128 k + ct is row u / 4, codes 16 (u % 4) ..
-          const unsigned char* gsrc = smem + S_E4 + e * kE4Group + (c % 3) * 4096;
-          unsigned char* slot = smem + S_F16 + f * kF16Slot;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int u = 128 * kk + ct, row = u >> 2, c16 = u & 3;
-            convert_unit(gsrc + (row >> 6) * (kE4Group / 2) + (row & 63) * 64 + 16 * c16, slot + row * 128, row, c16,
-                         true);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars[SB_F16FULL + f]);
-            if (c % 3 == 2) mbar_arrive(&bars[SB_E4EMPTY + e]);
-          }
-        }
       }
       if (!ok) give_up(p, abort_flag, smem, peer);
     } else {
@@ -391,10 +382,12 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       const int h = q * 32 + lane;
       const int j = (warp - 2) >> 2;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      // Q rows → TMEM as f16 pairs. Each head's row is first multiplied by a power of two
-      // 2^k_h that brings its largest magnitude into [2^14, 2^15), so that the bf16 →
-      // f16 conversion neither overflows nor goes subnormal for the elements that
-      // matter; 2^-k_h comes back in fp32 with the scores (heads beyond n_h are zero).
+      // Q rows → TMEM as two e4m3 parts. Each head's row is first multiplied by a power
+      // of two 2^k_h that brings its largest magnitude into [2^7, 2^8); then hi = e4m3(q)
+      // and lo = e4m3(q - hi). A bf16 value has 8 significant bits and e4m3 4, so
+      // hi + lo is the value exactly down to 2^-9 (e4m3's subnormal step), i.e. for every
+      // element within 2^-16 of the head's largest; 2^-k_h comes back in fp32 with the
+      // scores (heads beyond n_h are zero).
       const int qrows = p.n_h < 128 ? p.n_h : 128;
       const bool qok = warp_wait(&bars[SB_QFULL], 0, abort_flag);
       uint32_t qmax = 0;   // largest |q| of this thread's chunks, as bf16 magnitude bits
@@ -418,27 +411,40 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       // later writes of this region come after the first tile's vote (a barrier of the
       // same 256 threads), so these reads cannot see them
       const int qexp = (int)((qmax >> 7) & 0xFFu);   // biased bf16 exponent of max |q|
-      const int qk = qmax == 0u ? 0 : min(126, max(-126, 141 - qexp));
+      const int qk = qmax == 0u ? 0 : min(118, max(-126, 134 - qexp));
       const float qmul = __uint_as_float((uint32_t)(127 + qk) << 23);   // 2^k_h
-      const float qsl = __uint_as_float((uint32_t)(127 - qk) << 23) * scale_log2;   // 2^-k_h · scale · log2 e · 2^8
+      // 2^-k_h · scale · log2 e (scale_log2 carries the value side's 2^8, which the
+      // scores, taken on the codes' own values, do not need)
+      const float qsl = scalbnf(scale_log2, -qk - 8);
       if (qok) {
 #pragma unroll 1
         for (int c = j; c < 9; c += 2) {
-          uint32_t rg[32];
+          // 64 elements of chunk c: codes of element 4 w + b in byte b of column 16 c + w
+          uint32_t qh[16], ql[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) qh[w] = ql[w] = 0u;
           const unsigned char* row = smem + S_E4 + (c / 3) * kQGroup + (c % 3) * (qrows * 128) + h * 128;
 #pragma unroll
           for (int x = 0; x < 8; ++x) {
             uint4 v = h < p.n_h ? *reinterpret_cast<const uint4*>(row + ((x ^ (h & 7)) << 4))
                                 : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-              const __half2 hv = __floats2half2_rn(f2.x * qmul, f2.y * qmul);
-              rg[4 * x + e] = *reinterpret_cast<const uint32_t*>(&hv);
+              const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+              const float2 y = make_float2(f2.x * qmul, f2.y * qmul);
+              const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+              const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
+              const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+              const __nv_fp8x2_storage_t lo2 =
+                  __nv_cvt_float2_to_fp8x2(make_float2(y.x - hf.x, y.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+              const int pi = 4 * x + e;   // elements 2 pi, 2 pi + 1
+              qh[pi >> 1] |= (uint32_t)hi2 << (16 * (pi & 1));
+              ql[pi >> 1] |= (uint32_t)lo2 << (16 * (pi & 1));
             }
           }
-          MLA_TMEM_ST32(trow + kQCol + 32 * c, rg);
+          MLA_TMEM_ST16(trow + kQCol + 16 * c, qh);
+          MLA_TMEM_ST16(trow + kQLoCol + 16 * c, ql);
         }
         tmem_wait_st();
       } else {
@@ -777,13 +783,16 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
   cluster_sync();
 }
 
-// 3D map over rows of 576 e4m3 codes seen as (64 codes, row, 9 chunks of 64 codes),
-// no swizzle; a box of `box_rows` rows x `box_chunks` chunks lands chunk-major.
-bool make_code_map(const void* base, int64_t rows, int box_rows, int box_chunks, CUtensorMap* map) {
+// 3D map over rows of 576 e4m3 codes seen as (64 codes, row, 9 chunks of 64 codes); a
+// box of `box_rows` rows x `box_chunks` chunks lands chunk-major, each chunk a
+// [box_rows][64] block, 64B-swizzled for the score side's MMA operands or plain for the
+// value side's converters.
+bool make_code_map(const void* base, int64_t rows, int box_rows, int box_chunks, bool swizzle, CUtensorMap* map) {
   const uint64_t dims[3] = {64, (uint64_t)rows, (uint64_t)(kRow / 64)};
   const uint64_t strides[2] = {(uint64_t)kRow, 64};
   const uint32_t box[3] = {64, (uint32_t)box_rows, (uint32_t)box_chunks};
-  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box,
+                                swizzle ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
                       map);
 }
@@ -813,7 +822,10 @@ bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
 cudaError_t launch_decode_tc_fp8(const DecodeParams& p, cudaStream_t st) {
   const int rows = p.n_h < 128 ? p.n_h : 128;
   CUtensorMap e4s, e4v, qmap, omap;
-  if (!make_code_map(p.data, p.num_rows, 64, 3, &e4s) || !make_code_map(p.data, p.num_rows, 64, 8, &e4v) ||
+  // score side: 128 rows x 3 chunks per box (contiguous) or 64 rows x 1 chunk (a page)
+  const bool paged = p.block_table != nullptr;
+  if (!make_code_map(p.data, p.num_rows, paged ? 64 : kTile, paged ? 1 : 3, true, &e4s) ||
+      !make_code_map(p.data, p.num_rows, 64, 8, false, &e4v) ||
       !make_q_map(p.q_lat, (int64_t)p.B * p.n_h, rows, &qmap) ||
       !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 32 ? p.n_h : 32, &omap))
     return cudaErrorInvalidValue;

@@ -89,7 +89,7 @@ int mla_decode_kernel(int kv_dtype, int n_h) {
   p.n_h = n_h;
   p.num_rows = 1;
   if (!decode_tc_supported(p)) return -1;
-  return kv_dtype == MLA_KV_BF16 ? MLA_KERNEL_TC_BF16 : MLA_KERNEL_TC_F16_E4M3;
+  return kv_dtype == MLA_KV_BF16 ? MLA_KERNEL_TC_BF16 : MLA_KERNEL_TC_E4M3;
 }
 
 int mla_num_splits(int B, int max_seq_len, int n_h) {

@@ -21,7 +21,7 @@ int main(void) {
   if (mla_split_range(1000, 3, 1, &st, &en) != MLA_OK) return 1;
   if (mla_split_range(-1, 3, 1, &st, &en) != MLA_ERR_INVALID_ARG) return 2;
   if (mla_decode_kernel(MLA_KV_BF16, 128) != MLA_KERNEL_TC_BF16) return 3;
-  if (mla_decode_kernel(MLA_KV_FP8_E4M3, 128) != MLA_KERNEL_TC_F16_E4M3) return 4;
+  if (mla_decode_kernel(MLA_KV_FP8_E4M3, 128) != MLA_KERNEL_TC_E4M3) return 4;
   if (mla_decode_kernel(MLA_KV_BF16, 7) != -1) return 5;
   if (strncmp(mla_status_string(MLA_ERR_TIMEOUT), "MLA_ERR_TIMEOUT", 15) != 0) return 6;
   /* argument checks run on the host, before any CUDA call */

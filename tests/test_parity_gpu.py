@@ -135,7 +135,7 @@ def test_fp8_every_code_through_tensor_cores(cuda_device):
         codes = np.where(rng.random((L, 576)) < 0.5, rng.choice(sub, (L, 576)), rng.choice(finite, (L, 576)))
         scales = (rng.uniform(0.5, 1.0, L) / 448.0).astype(np.float32)
         case.set_codes(b, codes.astype(np.uint8), scales)
-    assert mla.decode_kernel("fp8", 128) == "tcgen05_f16_e4m3"
+    assert mla.decode_kernel("fp8", 128) == "tcgen05_e4m3"
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     out = case.run(n_splits=3, status=status)
     torch.cuda.synchronize()
