@@ -4,11 +4,12 @@
 //
 // Per head the absorbed query is a small GEMM with the latent dimension as M:
 //     q_lat[b, h, j] = sum_d W_UK[h, d, j] q^C[b, h, d]      (M = 512 j, N = batch, K = 128 d)
-// One CTA per (head, tile of up to 128 sequences). The four 32 KB M-tiles of W_UK[h]
-// (an MN-major operand: j is contiguous) and the batch tile of q^C arrive by TMA, each
-// M-tile on its own barrier so the tensor core starts on the first while the rest land;
-// tcgen05 accumulates four 128 x N fp32 tiles in TMEM and the epilogue rounds them to
-// bf16. The weight bytes dominate: W_UK is read from HBM once per call.
+// One CTA per (head, tile of up to 128 sequences, 128-row M-tile): the call is a single
+// short wave whose time is each CTA's load latency, so the weights are spread over four
+// times as many CTAs (two per SM) as heads. The 32 KB M-tile of W_UK[h] (an MN-major
+// operand: j is contiguous) and the batch tile of q^C arrive by TMA; tcgen05 accumulates
+// one 128 x N fp32 tile in TMEM and the epilogue rounds it to bf16. The weight bytes
+// dominate: W_UK is read from HBM once per call.
 //
 // The decoupled part is rotated on CUDA cores with the exactly reduced angles of
 // rope.cuh.
@@ -30,22 +31,23 @@ using namespace sm100;
 constexpr int kNB = 128;                     // sequences per CTA (the MMA N, padded to 16)
 constexpr int kThreads = 128;
 constexpr int kWTile = 2 * 128 * 128;        // one M-tile of W_UK[h]: two 64-j chunks x 128 d rows (32 KB)
-constexpr int OFF_W = 0;                     // four M-tiles
-constexpr int OFF_Q = 4 * kWTile;            // q^C tile: two 64-d chunks x 128 rows x 128 B
+constexpr int kMTiles = 4;                   // 512 latent dims = four 128-row M-tiles, one per CTA
+constexpr int OFF_W = 0;                     // this CTA's M-tile
+constexpr int OFF_Q = kWTile;                // q^C tile: two 64-d chunks x 128 rows x 128 B
 constexpr int OFF_BAR = OFF_Q + 2 * kNB * 128;
 constexpr int kSmem = OFF_BAR + 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
             const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int B, int n_h,
             const RopeTurns turns, __nv_bfloat16* __restrict__ q_lat) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int h = blockIdx.x, b0 = blockIdx.y * kNB;
+  const int h = blockIdx.x, b0 = blockIdx.y * kNB, mt = blockIdx.z;
   const int nb = min(kNB, B - b0);
   const int N = (nb + 15) & ~15;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [0..3] W M-tiles, [4] q tile, [5] MMAs done
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [0] W M-tile, [1] q tile, [2] MMAs done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 48);
   volatile int* ok_word = reinterpret_cast<volatile int*>(smem + OFF_BAR + 52);
   const bool aligned = (smem_u32(smem) & 1023u) == 0;   // the 128B swizzle needs 1024-byte aligned tiles
@@ -53,12 +55,12 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
 
   if (aligned) {
     if (threadIdx.x == 0) {
-      for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+      for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
       *ok_word = 0;
       fence_mbar_init_cluster();
     }
     if (warp == 0) {
-      tmem_alloc(tmem_slot, 512);
+      tmem_alloc(tmem_slot, 128);
       tmem_relinquish();
     }
   }
@@ -72,42 +74,40 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
       const uint64_t pol = l2_policy_evict_first();
       prefetch_tmap(&qmap);
       prefetch_tmap(&wmap);
-      for (int mt = 0; mt < 4; ++mt) {   // the weights do not depend on the previous kernel
-        mbar_arrive_expect_tx(&bars[mt], kWTile);
-        tma_load_3d(smem + OFF_W + mt * kWTile, &wmap, &bars[mt], 0, h * kNope, 2 * mt, pol);
-      }
+      // the weights do not depend on the previous kernel
+      mbar_arrive_expect_tx(&bars[0], kWTile);
+      tma_load_3d(smem + OFF_W, &wmap, &bars[0], 0, h * kNope, 2 * mt, pol);
       griddep_wait();
-      mbar_arrive_expect_tx(&bars[4], 2 * kNB * 128);
-      tma_load_4d(smem + OFF_Q, &qmap, &bars[4], 0, h, b0, 0, pol);
+      mbar_arrive_expect_tx(&bars[1], 2 * kNB * 128);
+      tma_load_4d(smem + OFF_Q, &qmap, &bars[1], 0, h, b0, 0, pol);
       const uint32_t idesc = idesc_f16(128, N, false, /*a_mn=*/true, /*b_mn=*/false);
       const volatile int never = 0;
-      bool ok = mbar_wait(&bars[4], 0, &never, kWaitNs);
-      for (int mt = 0; ok && mt < 4; ++mt) {
-        ok = mbar_wait(&bars[mt], 0, &never, kWaitNs);
-        if (!ok) break;
+      bool ok = mbar_wait(&bars[1], 0, &never, kWaitNs) && mbar_wait(&bars[0], 0, &never, kWaitNs);
+      if (ok) {
         tc_fence_after();
-        const uint32_t wt = smem_u32(smem + OFF_W + mt * kWTile);
+        const uint32_t wt = smem_u32(smem + OFF_W);
         const uint32_t qt = smem_u32(smem + OFF_Q);
 #pragma unroll
         for (int kk = 0; kk < kNope / 16; ++kk) {
           // A: 16 d rows of 128 B (64 j) per 64-j chunk, chunks 16 KB apart; B: q rows, K-major
           const uint64_t a = sdesc_sw128(wt + kk * 2048, 128 * 128, 1024);
           const uint64_t bq = sdesc_sw128(qt + (kk >> 2) * (kNB * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + 128 * mt, a, bq, idesc, kk > 0 ? 1u : 0u);
+          mma_ss(tmem, a, bq, idesc, kk > 0 ? 1u : 0u);
         }
       }
       *ok_word = ok ? 1 : 0;
-      mma_commit(&bars[5]);
+      mma_commit(&bars[2]);
       // loads still in flight land before the CTA may leave
-      mbar_wait(&bars[4], 0, &never, kWaitNs / 4);
-      for (int mt = 0; mt < 4; ++mt) mbar_wait(&bars[mt], 0, &never, kWaitNs / 4);
+      mbar_wait(&bars[1], 0, &never, kWaitNs / 4);
+      mbar_wait(&bars[0], 0, &never, kWaitNs / 4);
     }
 
     griddep_wait();   // q and pos may come from the previous kernel; q_lat may still be read by it
     // decoupled query, overlapping the tensor-core work: thread (n, g) rotates pairs
-    // 8g .. 8g+7 of sequence n; every load of a pass is issued before any math
+    // 8g .. 8g+7 of sequence n; every load of a pass is issued before any math. The four
+    // CTAs of a head share the batch tile's sequences, 32 at a time.
 #pragma unroll 1
-    for (int n0 = 0; n0 < nb; n0 += kThreads / 4) {
+    for (int n0 = (kThreads / 4) * mt; n0 < nb; n0 += kMTiles * (kThreads / 4)) {
       const int n = n0 + (threadIdx.x >> 2), g = threadIdx.x & 3;
       if (n < nb) {
         const int64_t row = (int64_t)(b0 + n) * n_h + h;
@@ -145,23 +145,20 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
 
     // epilogue: lane j of M-tile mt holds q_lat[b0 + n, h, 128 mt + j] in column n
     const volatile int never = 0;
-    const bool done = __all_sync(0xffffffffu, mbar_wait(&bars[5], 0, &never, kWaitNs));
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bars[2], 0, &never, kWaitNs));
     tc_fence_after();
     if (done && *ok_word) {
       const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+      const int j = 128 * mt + 32 * warp + lane;
 #pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        const int j = 128 * mt + 32 * warp + lane;
-#pragma unroll 1
-        for (int c0 = 0; c0 < N; c0 += 32) {
-          uint32_t r[32];
-          MLA_TMEM_LD32(trow + 128 * mt + c0, r);
-          tmem_wait_ld();
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t r[32];
+        MLA_TMEM_LD32(trow + c0, r);
+        tmem_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 32; ++x)
-            if (c0 + x < nb)
-              q_lat[((int64_t)(b0 + c0 + x) * n_h + h) * kRow + j] = __float2bfloat16_rn(__uint_as_float(r[x]));
-        }
+        for (int x = 0; x < 32; ++x)
+          if (c0 + x < nb)
+            q_lat[((int64_t)(b0 + c0 + x) * n_h + h) * kRow + j] = __float2bfloat16_rn(__uint_as_float(r[x]));
       }
     }
     tc_fence_before();
@@ -169,7 +166,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
   if (!aligned) griddep_wait();
   __syncthreads();
   tc_fence_after();
-  if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 512);
+  if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 128);
 }
 
 }  // namespace
@@ -201,7 +198,7 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, c
   static std::atomic<int> attr_done[kMaxDevices];
   const cudaError_t attr_err = smem_attr_once(absorb_q_tc, kSmem, attr_done);
   if (attr_err != cudaSuccess) return attr_err;
-  dim3 grid(n_h, ceil_div(B, kNB));
+  dim3 grid(n_h, ceil_div(B, kNB), kMTiles);
   return launch_overlapped(absorb_q_tc, grid, dim3(kThreads), kSmem, st, wmap, qmap, q, pos, B, n_h, turns, q_lat);
 }
 
