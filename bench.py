@@ -1,5 +1,5 @@
 #!/usr/bin/env python3
-"""Benchmark of one MLA decode step (absorb_q → decode_fwd → combine → up_v) on B300.
+"""Benchmark of one MLA decode step (absorb_q → decode_fwd → combine_up_v) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload all|NAME] [--no-cpu-baseline]
@@ -40,6 +40,7 @@ import workloads as W  # noqa: E402
 METRIC = "MLA decode latent-cache GB/s, tokens/s, % HBM roofline on 1 B300"
 HEADLINE = "v2_b32_l4096"
 L2_FLUSH_BYTES = 256 << 20
+N_CALLS = 3                                  # absorb_q, decode_fwd, combine_up_v
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # The oracle's bounded sample of each workload: (sequence, heads or None = all). The
@@ -266,8 +267,6 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         q_lat=torch.empty(B, n_h, 576, dtype=torch.bfloat16, device=dev),
         o_part=torch.empty(B, S, n_h, 512, dtype=torch.float32, device=dev),
         lse_part=torch.empty(B, S, n_h, dtype=torch.float32, device=dev),
-        o_lat=torch.empty(B, n_h, 512, dtype=torch.float32, device=dev),
-        lse=torch.empty(B, n_h, dtype=torch.float32, device=dev),
         o=torch.empty(B, n_h, 128, dtype=torch.float32, device=dev),
     )
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -292,13 +291,11 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         elif i == 1:
             mla.decode_fwd(bufs["q_lat"], cache, case.seq_lens, case.max_len, n_splits=0,
                            o_part=bufs["o_part"], lse_part=bufs["lse_part"])
-        elif i == 2:
-            mla.combine(bufs["o_part"], bufs["lse_part"], o_lat=bufs["o_lat"], lse=bufs["lse"])
-        else:
-            mla.up_v(bufs["o_lat"], case.w_uv, o=bufs["o"])
+        else:   # the merge of the split partials and W_UV, one launch; o only
+            mla.combine_up_v(bufs["o_part"], bufs["lse_part"], case.w_uv, o=bufs["o"])
 
     def step():
-        for i in range(4):
+        for i in range(N_CALLS):
             call(i)
 
     for _ in range(args.warmup):
@@ -306,12 +303,12 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     torch.cuda.synchronize()
 
     # The timed step is one CUDA-graph replay: an L2 flush (outside the timed interval),
-    # then the four library calls between two device-side events. Consecutive kernels of
+    # then the three library calls between two device-side events. Consecutive kernels of
     # the step overlap their launch and prologue with the previous kernel's tail
     # (programmatic dependent launch), so no event may sit between them in this graph;
     # a second graph with events between the calls gives the per-call breakdown.
     ev_step = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(N_CALLS + 1)]
     graph, graph_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
@@ -326,7 +323,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         with torch.cuda.graph(graph_parts, stream=cap):
             flush_l2()
             ev[0].record()
-            for i in range(4):
+            for i in range(N_CALLS):
                 call(i)
                 ev[i + 1].record()
     torch.cuda.current_stream().wait_stream(cap)
@@ -359,16 +356,16 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     for _ in range(K):
         graph_parts.replay()
         torch.cuda.synchronize()
-        per.append([ev[i].elapsed_time(ev[i + 1]) for i in range(4)])   # ms
+        per.append([ev[i].elapsed_time(ev[i + 1]) for i in range(N_CALLS)])   # ms
     per = np.array(per)
     step_ms = float(np.mean(steps))
     kern_ms = per.mean(axis=0)
     step_ms_max = dist.max(step_ms, dev)
 
     # e2e through the public API with host buffers: per step, H2D of the new queries
-    # (+ positions, lengths) from pinned memory, the four calls, and D2H of o. The
-    # headline form replays the step captured once as a CUDA graph (mla.DecodeStepGraph);
-    # the eager form makes the four Python calls every step (mla.decode_step).
+    # (+ positions, lengths) from pinned memory, the three calls, and D2H of o. The
+    # eager form makes the three Python calls every step (mla.decode_step); beside it,
+    # the step captured once as a CUDA graph (mla.DecodeStepGraph).
     h_q = case.q.cpu().pin_memory()
     h_pos = case.pos.cpu().pin_memory()
     h_len = case.seq_lens.cpu().pin_memory()
@@ -380,7 +377,8 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         d_q.copy_(h_q, non_blocking=True)
         d_pos.copy_(h_pos, non_blocking=True)
         d_len.copy_(h_len, non_blocking=True)
-        mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=0, bufs=e2e_bufs)
+        mla.decode_step(d_q, case.w_uk, case.w_uv, cache, d_len, d_pos, case.max_len, n_splits=0, bufs=e2e_bufs,
+                        latent=False)
         h_o.copy_(e2e_bufs["o"], non_blocking=True)
 
     g = mla.DecodeStepGraph(case.w_uk, case.w_uv, cache, B, case.max_len)
@@ -486,10 +484,9 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         "hbm_roofline_frac_step": round((cache_bytes + weight_bytes + io_bytes) / (step_ms / 1e3) / 1e9 / hbm_peak,
                                         4),
         "kernel_ms": {"absorb_q": round(float(kern_ms[0]), 5), "decode_fwd": round(decode_ms, 5),
-                      "combine": round(float(kern_ms[2]), 5), "up_v": round(float(kern_ms[3]), 5)},
+                      "combine_up_v": round(float(kern_ms[2]), 5)},
         "decode_kernel": mla.decode_kernel(w.kv, n_h),
         "roofline": roofline,
-        "cache_gbs_decode_combine": round(cache_bytes / ((decode_ms + float(kern_ms[2])) / 1e3) / 1e9, 1),
         "e2e": {"value": round(total_cache / (eager_mean / 1e3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(eager_mean, 5), "host_ms_per_step": round(float(np.mean(eager_host_ms)), 4),
                 "steps": len(eager_ms), "ms_median": round(float(np.median(eager_ms)), 5),
@@ -497,7 +494,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
                 "device_step_ratio": round(eager_mean / step_ms, 2),
                 "h2d_bytes_per_step": int(h_q.numel() * 2 + h_pos.numel() * 4 + h_len.numel() * 4),
                 "d2h_bytes_per_step": int(h_o.numel() * 4),
-                "path": "mla.decode_step (four Python calls over the C ABI) with H2D of q, pos and seq_lens from "
+                "path": "mla.decode_step (three Python calls over the C ABI) with H2D of q, pos and seq_lens from "
                         "pinned host buffers and D2H of o into a pinned buffer, every step",
                 "same_o_as_graph": same_o,
                 "graph": {"value": round(total_cache / (e2e_mean / 1e3) / 1e9, 2), "unit": "GB/s",
@@ -538,14 +535,15 @@ def run_ours(args, dist: Dist) -> dict | None:
         "vs_baseline": None, "dtype": head["dtype"],
         "data": "synthetic (seeded N(0,1) bf16 cache and queries, N(0,1/512) weights; no checkpoint)",
         **{k: v for k, v in head.items() if k not in ("metric", "value", "unit", "ms_per_step", "dtype")},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": N_CALLS * args.steps,
         "timing": "CUDA-graph replay of the step between two device-side events; kernel_ms from a second graph "
-                  "with events between the four calls (no launch overlap there, so they sum to more than the step)",
-        "step": "absorb_q + decode_fwd + combine + up_v, one MLA layer",
+                  "with events between the three calls (no launch overlap there, so they sum to more than the step)",
+        "step": "absorb_q + decode_fwd + combine_up_v (log-sum-exp merge of the splits and W_UV in one kernel), "
+                "one MLA layer",
     }
     if len(names) > 1:
         res["workloads"] = {n: recs[n] for n in names[1:]}
-        res["gpu_launches_all_workloads"] = 4 * args.steps * len(names)
+        res["gpu_launches_all_workloads"] = N_CALLS * args.steps * len(names)
     return res
 
 

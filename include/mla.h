@@ -19,6 +19,7 @@
  *   mla_decode_fwd split-KV attention of every head over the 576-wide cache rows
  *   mla_combine    log-sum-exp merge of the per-split partial results
  *   mla_up_v       o[b,h] = W_UV[h] o_lat[b,h]
+ *   mla_combine_up_v  the two calls above in one launch
  *
  * Conventions shared by every call
  *   - All pointers except `cache` (a host struct) are DEVICE pointers; the caller
@@ -199,6 +200,24 @@ MLA_API mla_status mla_combine(const float* o_part, const float* lse_part, int B
  */
 MLA_API mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h,
                     float* o, cudaStream_t stream);
+
+/*
+ * mla_combine_up_v — mla_combine and mla_up_v as one kernel launch.
+ *   ("DeepSeek-V2 机制拆解", §"长上下文推理的第一瓶颈": the weighted sum over the cached
+ *   latents, then W_UV; the split partials are merged as mla_combine defines.)
+ *   o[b,h,d] = sum_j W_UV[h,d,j] o_lat[b,h,j], with o_lat the merge of o_part's slots.
+ *   o_part [B, num_splits, n_h, 512] fp32, lse_part [B, num_splits, n_h] fp32 (as
+ *   mla_decode_fwd writes them), w_uv [n_h, 128, 512] bf16, o [B, n_h, 128] fp32 out.
+ *   o_lat [B, n_h, 512] fp32 and lse [B, n_h] fp32 are optional outputs (NULL: not
+ *   written); when given they hold mla_combine's results up to fp32 rounding order.
+ *   The merged o_lat never passes through memory on its way to W_UV.
+ *   Errors: NULL o_part, lse_part, w_uv or o, misalignment (16 bytes; lse 4 bytes),
+ *   B or num_splits out of range -> MLA_ERR_INVALID_ARG; n_h not 16/32/64/128 ->
+ *   MLA_ERR_UNSUPPORTED. o must not alias the inputs.
+ */
+MLA_API mla_status mla_combine_up_v(const float* o_part, const float* lse_part, int B,
+                            int num_splits, int n_h, const void* w_uv, float* o,
+                            float* o_lat, float* lse, cudaStream_t stream);
 
 /*
  * mla_cache_append — write the cache rows of T new tokens.

@@ -333,6 +333,26 @@ def up_v(o_lat, w_uv, o=None, stream=None):
     return o
 
 
+def combine_up_v(o_part, lse_part, w_uv, o=None, o_lat=None, lse=None, stream=None):
+    """combine + up_v in one launch (include/mla.h, mla_combine_up_v): o [B, n_h, 128]
+    from the split partials; o_lat and lse are written only when given."""
+    B, S, n_h = o_part.shape[0], o_part.shape[1], o_part.shape[2]
+    _need(o_part, "o_part", torch.float32, (B, S, n_h, D_LATENT))
+    _need(lse_part, "lse_part", torch.float32, (B, S, n_h))
+    _need(w_uv, "w_uv", torch.bfloat16, (n_h, D_NOPE, D_LATENT))
+    if o is None:
+        o = torch.empty(B, n_h, D_NOPE, dtype=torch.float32, device=o_part.device)
+    _need(o, "o", torch.float32, (B, n_h, D_NOPE))
+    if o_lat is not None:
+        _need(o_lat, "o_lat", torch.float32, (B, n_h, D_LATENT))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, n_h))
+    dev = _one_device(o_part=o_part, lse_part=lse_part, w_uv=w_uv, o=o, o_lat=o_lat, lse=lse)
+    _call("mla_combine_up_v", dev, _ptr(o_part), _ptr(lse_part), B, S, n_h, _ptr(w_uv), _ptr(o), _ptr(o_lat),
+          _ptr(lse), stream=stream)
+    return o, o_lat, lse
+
+
 def cache_append(h, w_dkv, w_kr, seq_ids, pos, cache: Cache, num_seqs: int | None = None,
                  rope_base: float = 10000.0, staging=None, status=None, stream=None, yarn: Yarn | None = None):
     """Write the cache rows of the new tokens (include/mla.h, mla_cache_append):
@@ -381,15 +401,25 @@ def quantize_fp8(rows, codes=None, scales=None, stream=None):
 
 def decode_step(q, w_uk, w_uv, cache: Cache, seq_lens, pos, max_seq_len: int, n_splits: int = 0,
                 softmax_scale: float | None = None, rope_base: float = 10000.0, bufs: dict | None = None,
-                status=None, stream=None, yarn: Yarn | None = None):
-    """All four calls of one decode step; `bufs` (optional) holds preallocated outputs."""
+                status=None, stream=None, yarn: Yarn | None = None, latent: bool = True):
+    """One decode step: absorb_q, decode_fwd, then combine and up_v as one launch
+    (combine_up_v). `bufs` (optional) holds preallocated outputs. With latent=False the
+    merged o_lat and lse are not written (None in the result)."""
     bufs = {} if bufs is None else bufs
     q_lat = absorb_q(q, w_uk, pos, q_lat=bufs.get("q_lat"), rope_base=rope_base, stream=stream, yarn=yarn)
     o_part, lse_part = decode_fwd(q_lat, cache, seq_lens, max_seq_len, softmax_scale, n_splits,
                                   o_part=bufs.get("o_part"), lse_part=bufs.get("lse_part"), status=status,
                                   stream=stream)
-    o_lat, lse = combine(o_part, lse_part, o_lat=bufs.get("o_lat"), lse=bufs.get("lse"), stream=stream)
-    o = up_v(o_lat, w_uv, o=bufs.get("o"), stream=stream)
+    o_lat = lse = None
+    if latent:
+        B, n_h = q_lat.shape[0], q_lat.shape[1]
+        o_lat = bufs.get("o_lat")
+        if o_lat is None:
+            o_lat = torch.empty(B, n_h, D_LATENT, dtype=torch.float32, device=q_lat.device)
+        lse = bufs.get("lse")
+        if lse is None:
+            lse = torch.empty(B, n_h, dtype=torch.float32, device=q_lat.device)
+    o, o_lat, lse = combine_up_v(o_part, lse_part, w_uv, o=bufs.get("o"), o_lat=o_lat, lse=lse, stream=stream)
     return dict(q_lat=q_lat, o_part=o_part, lse_part=lse_part, o_lat=o_lat, lse=lse, o=o)
 
 
@@ -400,7 +430,7 @@ def decode_multi(q, w_uk, w_uv, cache: Cache, seq_lens, max_seq_len: int, n_spli
     cached tokens of sequence b are its new ones, query j sits at position L_b - T + j and
     sees tokens 0 .. L_b - T + j. q [B, T, n_h, 192] bf16 → dict of the step's outputs
     with o [B, T, n_h, 128]. The library builds a paged view of the cache with one
-    sequence per query and runs the four calls on it."""
+    sequence per query and runs the decode step on it."""
     B, T, n_h = q.shape[0], q.shape[1], q.shape[2]
     _need(q, "q", torch.bfloat16, (B, T, n_h, D_Q))
     _need(seq_lens, "seq_lens", torch.int32, (B,))
@@ -429,10 +459,11 @@ class DecodeStepGraph:
     """One decode step of one layer, captured once as a CUDA graph and replayed per step.
 
     A serving loop repeats the same step on the same buffers, so the host work of the
-    four calls (argument checks, tensor maps, launches) is paid once, at capture. The
+    three calls (argument checks, tensor maps, launches) is paid once, at capture. The
     graph holds, in order: the copy of the step's inputs from pinned host buffers
-    (`h_q`, `h_pos`, `h_seq_lens`, which the caller fills before each step), the four
-    C-ABI calls, and the copy of `o` into the pinned host buffer `h_o`.
+    (`h_q`, `h_pos`, `h_seq_lens`, which the caller fills before each step), the C-ABI
+    calls of decode_step, and the copy of `o` into the pinned host buffer `h_o`. With
+    latent=True the step also writes the merged `bufs["o_lat"]` and `bufs["lse"]`.
 
         g = DecodeStepGraph(w_uk, w_uv, cache, B, max_seq_len)
         g.h_q.copy_(...); g.h_pos.copy_(...); g.h_seq_lens.copy_(...)
@@ -445,7 +476,7 @@ class DecodeStepGraph:
 
     def __init__(self, w_uk, w_uv, cache: Cache, B: int, max_seq_len: int, n_splits: int = 0,
                  softmax_scale: float | None = None, rope_base: float = 10000.0, status=None,
-                 yarn: Yarn | None = None):
+                 yarn: Yarn | None = None, latent: bool = False):
         n_h = w_uk.shape[0]
         dev = w_uk.device
         self.device, self.B, self.n_h = dev, B, n_h
@@ -461,14 +492,15 @@ class DecodeStepGraph:
             q_lat=torch.empty(B, n_h, D_ROW, dtype=torch.bfloat16, device=dev),
             o_part=torch.empty(B, S, n_h, D_LATENT, dtype=torch.float32, device=dev),
             lse_part=torch.empty(B, S, n_h, dtype=torch.float32, device=dev),
-            o_lat=torch.empty(B, n_h, D_LATENT, dtype=torch.float32, device=dev),
-            lse=torch.empty(B, n_h, dtype=torch.float32, device=dev),
             o=torch.empty(B, n_h, D_NOPE, dtype=torch.float32, device=dev))
+        if latent:
+            self.bufs["o_lat"] = torch.empty(B, n_h, D_LATENT, dtype=torch.float32, device=dev)
+            self.bufs["lse"] = torch.empty(B, n_h, dtype=torch.float32, device=dev)
         self.stream = torch.cuda.Stream(dev)
         self.graph = torch.cuda.CUDAGraph()
         args = (w_uk, w_uv, cache, self.d_seq_lens, self.d_pos, max_seq_len)
         kw = dict(n_splits=n_splits, softmax_scale=softmax_scale, rope_base=rope_base, bufs=self.bufs, status=status,
-                  yarn=yarn)
+                  yarn=yarn, latent=latent)
         with torch.cuda.device(dev), torch.cuda.stream(self.stream):
             # one eager step first: every argument check and launch path runs once outside capture
             decode_step(self.d_q, *args, **kw)

@@ -27,7 +27,7 @@ EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
     "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version", "mla_decode_kernel",
     "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append", "mla_absorb_q_ex",
-    "mla_cache_append_ex", "mla_multi_token_view",
+    "mla_cache_append_ex", "mla_multi_token_view", "mla_combine_up_v",
 ]
 
 
@@ -77,6 +77,7 @@ def _load():
     lib.mla_test_decode_stalled.argtypes = [vp, ctypes.POINTER(MlaCache), vp, i32, i32, i32, f32, i32, vp, vp, vp,
                                             ctypes.c_uint64, vp]
     lib.mla_up_v.argtypes = [vp, vp, i32, i32, vp, vp]
+    lib.mla_combine_up_v.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, ctypes.POINTER(MlaCache), i32, vp, vp, vp]
     lib.mla_cache_append_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, ctypes.POINTER(MlaRope),
                                         ctypes.POINTER(MlaCache), i32, vp, vp, vp]
@@ -92,7 +93,7 @@ def _load():
     for fn in ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
                "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel",
                "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append", "mla_absorb_q_ex",
-               "mla_cache_append_ex", "mla_multi_token_view"):
+               "mla_cache_append_ex", "mla_multi_token_view", "mla_combine_up_v"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 

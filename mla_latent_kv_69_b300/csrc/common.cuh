@@ -94,6 +94,9 @@ cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, in
                         cudaStream_t st);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int S, int n_h,
                            float* o_lat, float* lse, cudaStream_t st);
+// combine and up_v in one kernel; o_lat and lse may be null (not written)
+cudaError_t launch_combine_up_v(const float* o_part, const float* lse_part, int S, const __nv_bfloat16* w_uv, int B,
+                                int n_h, float* o, float* o_lat, float* lse, cudaStream_t st);
 cudaError_t launch_cache_append(const __nv_bfloat16* h, const __nv_bfloat16* w_dkv, const __nv_bfloat16* w_kr,
                                 const int32_t* seq_ids, const int32_t* pos, int T, int d, const RopeSpec& rope,
                                 const mla_cache& cache, int num_seqs, __nv_bfloat16* staging, int32_t* status,

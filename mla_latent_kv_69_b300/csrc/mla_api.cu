@@ -234,6 +234,18 @@ mla_status mla_up_v(const float* o_lat, const void* w_uv, int B, int n_h, float*
   return cuda_status(launch_up_v(o_lat, static_cast<const __nv_bfloat16*>(w_uv), B, n_h, o, stream));
 }
 
+mla_status mla_combine_up_v(const float* o_part, const float* lse_part, int B, int num_splits, int n_h,
+                            const void* w_uv, float* o, float* o_lat, float* lse, cudaStream_t stream) {
+  if (!o_part || !lse_part || !w_uv || !o) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
+  if (o_lat && !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxBatch || num_splits < 1 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (!valid_heads(n_h)) return n_h > 0 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_up_v(o_part, lse_part, num_splits, static_cast<const __nv_bfloat16*>(w_uv), B,
+                                         n_h, o, o_lat, lse, stream));
+}
+
 mla_status mla_cache_append(const void* h, const void* w_dkv, const void* w_kr, const int32_t* seq_ids,
                             const int32_t* pos, int T, int d_model, float rope_base, const mla_cache* cache,
                             int num_seqs, void* staging, int32_t* status, cudaStream_t stream) {

@@ -331,6 +331,7 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo) {
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                       \
       : "memory")
 
+// 32 lanes x 32 bits, 16 columns (half of MLA_TMEM_LD32).
 #define MLA_TMEM_ST16(taddr, r)                                                                                \
   asm volatile(                                                                                                \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" \
@@ -386,14 +387,6 @@ __device__ __forceinline__ uint32_t named_popc(uint32_t id, uint32_t count, bool
       : "memory");
   return r;
 }
-// 32 lanes x 32 bits, 16 columns (half of MLA_TMEM_LD32).
-#define MLA_TMEM_ST16(taddr, r)                                                                         \
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
-               "%13,%14,%15,%16};" ::"r"(taddr),                                                        \
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),  \
-               "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),        \
-               "r"(r[15])                                                                               \
-               : "memory")
 }  // namespace sm100
 }  // namespace mla
 

@@ -9,6 +9,9 @@
 // core takes bf16, so each fp32 value is split as hi = bf16(x), lo = bf16(x - hi) and
 // both halves enter the same MMA as 2 x N columns (W·hi + W·lo carries ~16
 // significant bits of o_lat instead of 8). The epilogue adds the two column halves.
+// A second instance merges the split partials itself (mla_combine_up_v): the threads form
+// each sequence's log-sum-exp weights, then build the operand rows as the weighted sums
+// of the slots, so the merge costs no launch and o_lat no round trip through memory.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -24,19 +27,25 @@ namespace {
 using namespace sm100;
 
 constexpr int kNB = 32;                      // sequences per CTA; MMA N = 2 x round16(nb) <= 64
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;                // eight warps stage the operand; the epilogue splits the columns
 constexpr int kChunks = kLatent / 64;        // 8 K-chunks of 64 j
 constexpr int kWBox = 2 * kNope * 128;       // two chunks of W_UV[h]: 128 d rows x 128 j (32 KB)
 constexpr int kXChunk = 2 * kNB * 128;       // one chunk of the (hi, lo) rows: up to 64 rows x 64 j (8 KB)
 constexpr int OFF_W = 0;                     // four boxes = all of W_UV[h]
 constexpr int OFF_X = 4 * kWBox;             // eight chunks
-constexpr int OFF_BAR = OFF_X + kChunks * kXChunk;
+constexpr int kMaxFusedSlots = MLA_MAX_SPLITS;   // the merge's weights: kNB sequences x every slot (32 KB)
+constexpr int OFF_CW = OFF_X + kChunks * kXChunk;
+constexpr int OFF_BAR = OFF_CW + kNB * kMaxFusedSlots * 4;
 constexpr int kSmem = OFF_BAR + 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
+// kMerge: the operand is merged from the split partials on the fly (mla_combine's
+// log-sum-exp merge) instead of read from o_lat; o_lat and lse are then written as
+// by-products when their pointers are given.
+template <bool kMerge>
 __global__ void __launch_bounds__(kThreads, 1)
-up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_lat, int B, int n_h,
-        float* __restrict__ o) {
+up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_lat, const float* __restrict__ lse_part,
+        int S, int B, int n_h, float* __restrict__ o, float* __restrict__ o_lat_out, float* __restrict__ lse_out) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int h = blockIdx.x, b0 = blockIdx.y * kNB;
   const int nb = min(kNB, B - b0);
@@ -77,46 +86,99 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
         tma_load_3d(smem + OFF_W + i * kWBox, &wmap, &bars[i], 0, h * kNope, 2 * i, pol);
       }
     }
-    griddep_wait();   // o_lat comes from the previous kernel
-    // o_lat rows → bf16 hi/lo rows of every chunk (K-major, 128B swizzle); rows past nb
-    // are zero. Item (n, c, qc) covers columns 64 c + 8 qc .. +8 of sequence n.
-    constexpr int kUnroll = 4;
+    griddep_wait();   // o_lat (or the partials) come from the previous kernel
+    float* cw = reinterpret_cast<float*>(smem + OFF_CW);   // [n][s] merge weights
+    if constexpr (kMerge) {
+      // per sequence: m = max_s lse_s, w_s = exp(lse_s - m) / sum_s exp(lse_s - m);
+      // slots with lse = -inf weigh 0, a sequence without any gives o_lat = 0, lse = -inf
+      for (int n = threadIdx.x; n < nb; n += kThreads) {
+        const float* lp = lse_part + (int64_t)(b0 + n) * S * n_h + h;
+        float m = -INFINITY;
+        for (int sl = 0; sl < S; ++sl) m = fmaxf(m, lp[(int64_t)sl * n_h]);
+        float z = 0.f;
+        for (int sl = 0; sl < S; ++sl) {
+          const float l = lp[(int64_t)sl * n_h];
+          const float wgt = (m == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - m);
+          cw[n * kMaxFusedSlots + sl] = wgt;
+          z += wgt;
+        }
+        const float inv = z > 0.f ? 1.f / z : 0.f;
+        for (int sl = 0; sl < S; ++sl) cw[n * kMaxFusedSlots + sl] *= inv;
+        if (lse_out) lse_out[(int64_t)(b0 + n) * n_h + h] = z > 0.f ? m + logf(z) : -INFINITY;
+      }
+      __syncthreads();
+    }
+    // o_lat rows → bf16 hi/lo rows of every chunk (K-major, 128B swizzle). Item idx is
+    // one float4 of a valid row: sequence n = idx / 128, columns 4 (idx % 128) .. +4.
+    // Merged, it is the weighted sum over the slots; else the slot is o_lat itself.
+    constexpr int kU = 4;                      // items per thread in flight
+    constexpr int kS = kMerge ? 4 : 1;         // slots per item in flight
+    const int items = nb * 128;
+    const int64_t row_stride = (int64_t)S * n_h * kLatent;   // floats from sequence b to b + 1
 #pragma unroll 1
-    for (int base = threadIdx.x; base < NP * 64; base += kThreads * kUnroll) {
-      float4 v[kUnroll][2];
+    for (int base = threadIdx.x; base < items; base += kThreads * kU) {
+      float4 acc[kU];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int idx = base + u * kThreads;
-        const int n = idx >> 6;
-        if (idx < NP * 64 && n < nb) {
-          const float4* src = reinterpret_cast<const float4*>(o_lat + ((int64_t)(b0 + n) * n_h + h) * kLatent) +
-                              2 * (idx & 63);
-          v[u][0] = src[0];
-          v[u][1] = src[1];
-        } else {
-          v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+      for (int s0 = 0; s0 < S; s0 += kS) {
+        float4 a[kU][kS];
+        float wt[kU][kS];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int idx = base + u * kThreads;
+          const int n = idx >> 7;
+#pragma unroll
+          for (int k = 0; k < kS; ++k) {
+            const int sl = s0 + k;
+            const bool valid = idx < items && sl < S;
+            wt[u][k] = valid ? (kMerge ? cw[n * kMaxFusedSlots + sl] : 1.f) : 0.f;
+            a[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (wt[u][k] != 0.f) {
+              const float4* src = reinterpret_cast<const float4*>(o_lat + (b0 + n) * row_stride +
+                                                                  ((int64_t)sl * n_h + h) * kLatent) +
+                                  (idx & 127);
+              a[u][k] = kMerge ? __ldcs(src) : *src;
+            }
+          }
         }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int k = 0; k < kS; ++k) {
+            acc[u].x = fmaf(wt[u][k], a[u][k].x, acc[u].x);
+            acc[u].y = fmaf(wt[u][k], a[u][k].y, acc[u].y);
+            acc[u].z = fmaf(wt[u][k], a[u][k].z, acc[u].z);
+            acc[u].w = fmaf(wt[u][k], a[u][k].w, acc[u].w);
+          }
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const int idx = base + u * kThreads;
-        if (idx >= NP * 64) continue;
-        const int n = idx >> 6, c = (idx >> 3) & 7, qc = idx & 7;
-        const float x[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-          const float2 hf = __bfloat1622float2(hv);
-          const __nv_bfloat162 lv = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
-          hi[e] = *reinterpret_cast<const uint32_t*>(&hv);
-          lo[e] = *reinterpret_cast<const uint32_t*>(&lv);
-        }
-        unsigned char* xs = smem + OFF_X + c * kXChunk;
+        if (idx >= items) continue;
+        const int n = idx >> 7, f4 = idx & 127;
+        if (kMerge && o_lat_out)
+          reinterpret_cast<float4*>(o_lat_out + ((int64_t)(b0 + n) * n_h + h) * kLatent)[f4] = acc[u];
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+        const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+        const __nv_bfloat162 l0 = __floats2bfloat162_rn(acc[u].x - f0.x, acc[u].y - f0.y);
+        const __nv_bfloat162 l1 = __floats2bfloat162_rn(acc[u].z - f1.x, acc[u].w - f1.y);
+        // column 4 f4 sits in chunk f4 / 16, 16-byte unit (f4 / 2) % 8, half f4 % 2
+        const int c = f4 >> 4, qc = (f4 >> 1) & 7, half = f4 & 1;
+        unsigned char* xs = smem + OFF_X + c * kXChunk + 8 * half;
         const int rh = n, rl = NP + n;
-        *reinterpret_cast<uint4*>(xs + rh * 128 + ((qc ^ (rh & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(xs + rl * 128 + ((qc ^ (rl & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint2*>(xs + rh * 128 + ((qc ^ (rh & 7)) << 4)) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+        *reinterpret_cast<uint2*>(xs + rl * 128 + ((qc ^ (rl & 7)) << 4)) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
       }
+    }
+    // rows nb .. NP - 1 of both halves are zero: (NP - nb) rows x 2 halves x 8 chunks x 128 B
+    for (int z = threadIdx.x; z < (NP - nb) * 2 * kChunks * 8; z += kThreads) {
+      const int unit = z & 7, c = (z >> 3) & 7, r2 = z >> 6;
+      const int r = (r2 >> 1) + nb + ((r2 & 1) ? NP : 0);
+      *reinterpret_cast<uint4*>(smem + OFF_X + c * kXChunk + r * 128 + unit * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
     mbar_arrive(&bars[4]);
@@ -140,14 +202,17 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
       for (int i = 0; i < 4; ++i) mbar_wait(&bars[i], 0, &never, kWaitNs / 4);
     }
     __syncthreads();   // orders ok_word
-    // epilogue: lane d holds W_UV[h, d, :] · hi in column n and · lo in column NP + n
+    // epilogue: lane d holds W_UV[h, d, :] · hi in column n and · lo in column NP + n;
+    // warp w reads TMEM lanes 32 (w % 4) .. +32 (its lane quarter), column groups of 16
+    // alternating between warps w and w + 4
     const bool done = __all_sync(0xffffffffu, mbar_wait(&bars[5], 0, &never, kWaitNs));
     tc_fence_after();
     if (done && *ok_word) {
-      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-      const int d = 32 * warp + lane;
+      const int quarter = warp & 3;
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+      const int d = 32 * quarter + lane;
 #pragma unroll 1
-      for (int c0 = 0; c0 < NP; c0 += 16) {
+      for (int c0 = 16 * (warp >> 2); c0 < NP; c0 += 32) {
         uint32_t rh[16], rl[16];
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                      : "=r"(rh[0]), "=r"(rh[1]), "=r"(rh[2]), "=r"(rh[3]), "=r"(rh[4]), "=r"(rh[5]), "=r"(rh[6]),
@@ -174,24 +239,43 @@ up_v_tc(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ o_la
   if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 64);
 }
 
+
+// W_UV viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = 128 d rows x two chunks
+bool wuv_map(const __nv_bfloat16* w_uv, int n_h, CUtensorMap* wmap) {
+  const uint64_t dims[3] = {64, (uint64_t)n_h * kNope, kChunks};
+  const uint64_t strides[2] = {(uint64_t)kLatent * 2, 128};
+  const uint32_t box[3] = {64, kNope, 2};
+  return encode_tiled(tmap_desc(w_uv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      wmap);
+}
+
 }  // namespace
 
 cudaError_t launch_up_v(const float* o_lat, const __nv_bfloat16* w_uv, int B, int n_h, float* o,
                         cudaStream_t st) {
-  // W_UV viewed as (64 j, row n_h*128 + d, 8 chunks of 64 j); box = 128 d rows x two chunks
   CUtensorMap wmap;
-  const uint64_t dims[3] = {64, (uint64_t)n_h * kNope, kChunks};
-  const uint64_t strides[2] = {(uint64_t)kLatent * 2, 128};
-  const uint32_t box[3] = {64, kNope, 2};
-  if (!encode_tiled(tmap_desc(w_uv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
-                    &wmap))
-    return cudaErrorInvalidValue;
+  if (!wuv_map(w_uv, n_h, &wmap)) return cudaErrorInvalidValue;
   static std::atomic<int> attr_done[kMaxDevices];
-  const cudaError_t attr_err = smem_attr_once(up_v_tc, kSmem, attr_done);
+  const cudaError_t attr_err = smem_attr_once(up_v_tc<false>, kSmem, attr_done);
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(n_h, ceil_div(B, kNB));
-  return launch_overlapped(up_v_tc, grid, dim3(kThreads), kSmem, st, wmap, o_lat, B, n_h, o);
+  return launch_overlapped(up_v_tc<false>, grid, dim3(kThreads), kSmem, st, wmap, o_lat, (const float*)nullptr, 1, B,
+                           n_h, o, (float*)nullptr, (float*)nullptr);
+}
+
+cudaError_t launch_combine_up_v(const float* o_part, const float* lse_part, int S, const __nv_bfloat16* w_uv, int B,
+                                int n_h, float* o, float* o_lat, float* lse, cudaStream_t st) {
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
+  if (S < 1 || S > kMaxFusedSlots) return cudaErrorInvalidValue;
+  CUtensorMap wmap;
+  if (!wuv_map(w_uv, n_h, &wmap)) return cudaErrorInvalidValue;
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t attr_err = smem_attr_once(up_v_tc<true>, kSmem, attr_done);
+  if (attr_err != cudaSuccess) return attr_err;
+  dim3 grid(n_h, ceil_div(B, kNB));
+  return launch_overlapped(up_v_tc<true>, grid, dim3(kThreads), kSmem, st, wmap, o_part, lse_part, S, B, n_h, o,
+                           o_lat, lse);
 }
 
 }  // namespace mla

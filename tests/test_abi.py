@@ -127,6 +127,14 @@ def test_other_calls_reject_bad_arguments_on_host():
     assert L.mla_combine(A, A, 1, 1, 128, None, None, None) == INVALID
     assert L.mla_up_v(A, A, 1, 100, A, None) == UNSUPPORTED
     assert L.mla_up_v(A, None, 1, 128, A, None) == INVALID
+    assert L.mla_combine_up_v(A, A, 2, 0, 128, A, A, None, None, None) == INVALID
+    assert L.mla_combine_up_v(A, A, 2, 257, 128, A, A, None, None, None) == INVALID
+    assert L.mla_combine_up_v(A, A, 0, 3, 128, A, A, None, None, None) == INVALID
+    assert L.mla_combine_up_v(A, A, 2, 3, 100, A, A, None, None, None) == UNSUPPORTED
+    assert L.mla_combine_up_v(A, A, 2, 3, 128, None, A, None, None, None) == INVALID
+    assert L.mla_combine_up_v(A, A, 2, 3, 128, A, None, None, None, None) == INVALID
+    assert L.mla_combine_up_v(A, A, 2, 3, 128, A, A, MIS, None, None) == INVALID     # o_lat misaligned
+    assert L.mla_combine_up_v(A, A, 2, 3, 128, A, A, None, A + 2, None) == INVALID   # lse misaligned
     assert L.mla_quantize_fp8(A, -1, A, A, None) == INVALID
     assert L.mla_quantize_fp8(MIS, 10, A, A, None) == INVALID
     assert L.mla_quantize_fp8(A, 0, A, A, None) == _lib.MLA_OK      # nothing to do

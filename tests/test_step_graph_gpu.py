@@ -1,6 +1,6 @@
 """mla.DecodeStepGraph: the decode step captured once as a CUDA graph (copies of the
-step's inputs from pinned host buffers, the four C-ABI calls, the copy of o back) gives,
-replay after replay, exactly what the eager four-call step gives on the same inputs, and
+step's inputs from pinned host buffers, the C-ABI calls of decode_step, the copy of o back) gives,
+replay after replay, exactly what the eager step gives on the same inputs, and
 takes each step's inputs from the host buffers as they are at replay time."""
 
 import numpy as np
