@@ -332,36 +332,9 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         graph_parts.replay()
     torch.cuda.synchronize()
 
-    K = args.steps
-    sampler = ClockSampler(dist.local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    sampler.start()
-    # Keep the GPU under this load for a while so nvidia-smi's 200 ms samples cover it;
-    # the timed steps follow immediately inside the same sampling window.
-    t_soak = time.perf_counter()
-    while time.perf_counter() - t_soak < args.soak:
-        for _ in range(20):
-            graph.replay()
-        torch.cuda.synchronize()
-    dist.barrier()
-    torch.cuda.synchronize()
-    steps = []
-    for _ in range(K):
-        graph.replay()
-        torch.cuda.synchronize()
-        steps.append(ev_step[0].elapsed_time(ev_step[1]))   # ms
-    torch.cuda.synchronize()
-    dist.barrier()
-    clocks = sampler.stop()
-    per = []
-    for _ in range(K):
-        graph_parts.replay()
-        torch.cuda.synchronize()
-        per.append([ev[i].elapsed_time(ev[i + 1]) for i in range(N_CALLS)])   # ms
-    per = np.array(per)
-    step_ms = float(np.mean(steps))
-    kern_ms = per.mean(axis=0)
-    step_ms_max = dist.max(step_ms, dev)
-
+    # The e2e and cache-write timings come before the clock-sampling window: host API
+    # calls of this process ran several times slower for a few hundred ms after the
+    # nvidia-smi sampler stopped, which would charge the sampler to the library.
     # e2e through the public API with host buffers: per step, H2D of the new queries
     # (+ positions, lengths) from pinned memory, the three calls, and D2H of o. The
     # eager form makes the three Python calls every step (mla.decode_step); beside it,
@@ -391,7 +364,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
             run()
         torch.cuda.synchronize()
         e2e_ms, host_ms = [], []
-        for _ in range(max(K, 30)):
+        for _ in range(max(args.steps, 30)):
             flush_l2()
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -425,7 +398,7 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
         mla.cache_append(h_new, w_dkv, w_kr, a_seq, a_pos, cache, staging=a_stage)
     torch.cuda.synchronize()
     app_ms = []
-    for _ in range(K):
+    for _ in range(args.steps):
         flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -437,6 +410,37 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
     row_bytes = 576 * 2 if w.kv == "bf16" else 576 + 4 + 2 * 576 * 2   # e4m3: codes + scale, staging out and in
     app_bytes = 576 * d_model * 2 + B * d_model * 2 + B * row_bytes
     del h_new, w_dkv, w_kr, a_seq, a_pos, a_stage
+
+    K = args.steps
+    sampler = ClockSampler(dist.local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    # Keep the GPU under this load for a while so nvidia-smi's 200 ms samples cover it;
+    # the timed steps follow immediately inside the same sampling window.
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        for _ in range(20):
+            graph.replay()
+        torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    steps = []
+    for _ in range(K):
+        graph.replay()
+        torch.cuda.synchronize()
+        steps.append(ev_step[0].elapsed_time(ev_step[1]))   # ms
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    per = []
+    for _ in range(K):
+        graph_parts.replay()
+        torch.cuda.synchronize()
+        per.append([ev[i].elapsed_time(ev[i + 1]) for i in range(N_CALLS)])   # ms
+    per = np.array(per)
+    step_ms = float(np.mean(steps))
+    kern_ms = per.mean(axis=0)
+    step_ms_max = dist.max(step_ms, dev)
+
 
     peaks, peaks_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -501,7 +505,8 @@ def measure_ours(name: str, args, dist: Dist, headline: bool) -> dict:
                           "ms_per_step": round(e2e_mean, 5),
                           "host_ms_per_step": round(float(np.mean(host_ms)), 4),
                           "ms_median": round(float(np.median(e2e_ms)), 5),
-                          "path": "mla.DecodeStepGraph.replay: the same copies and calls captured once"}},
+                          "path": "mla.DecodeStepGraph.replay: the same copies around the three calls captured "
+                                  "once as a CUDA graph"}},
         "cache_append": {"ms": round(app_mean, 5), "tokens": B, "d_model": d_model,
                          "algorithmic_bytes": int(app_bytes),
                          "achieved_gbs": round(app_bytes / (app_mean / 1e3) / 1e9, 1),
