@@ -6,7 +6,9 @@
 //     q_lat[b, h, j] = sum_d W_UK[h, d, j] q^C[b, h, d]      (M = 512 j, N = batch, K = 128 d)
 // One CTA per (head, tile of up to 128 sequences, 128-row M-tile): the call is a single
 // short wave whose time is each CTA's load latency, so the weights are spread over four
-// times as many CTAs (two per SM) as heads. The 32 KB M-tile of W_UK[h] (an MN-major
+// times as many CTAs as heads. The query tile, shared memory and TMEM are sized for the
+// batch (N sequences, a multiple of 16), so that up to four CTAs fit on an SM and the
+// 4 n_h CTAs of a small batch run in one wave. The 32 KB M-tile of W_UK[h] (an MN-major
 // operand: j is contiguous) and the batch tile of q^C arrive by TMA; tcgen05 accumulates
 // one 128 x N fp32 tile in TMEM and the epilogue rounds it to bf16. The weight bytes
 // dominate: W_UK is read from HBM once per call.
@@ -28,28 +30,38 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kNB = 128;                     // sequences per CTA (the MMA N, padded to 16)
+constexpr int kNB = 128;                     // at most this many sequences per CTA (the MMA N)
 constexpr int kThreads = 128;
 constexpr int kWTile = 2 * 128 * 128;        // one M-tile of W_UK[h]: two 64-j chunks x 128 d rows (32 KB)
 constexpr int kMTiles = 4;                   // 512 latent dims = four 128-row M-tiles, one per CTA
 constexpr int OFF_W = 0;                     // this CTA's M-tile
-constexpr int OFF_Q = kWTile;                // q^C tile: two 64-d chunks x 128 rows x 128 B
-constexpr int OFF_BAR = OFF_Q + 2 * kNB * 128;
-constexpr int kSmem = OFF_BAR + 64;
+constexpr int OFF_Q = kWTile;                // q^C tile: two 64-d chunks x nbox rows x 128 B
+constexpr int kBarBytes = 64;                // barriers, TMEM slot and flag after the q^C tile
+constexpr int kSmemMax = OFF_Q + 2 * kNB * 128 + kBarBytes;
+
+// rows of the q^C box (and MMA N bound) for a batch of B: a multiple of 16, at most kNB
+inline int q_box_rows(int B) { return B >= kNB ? kNB : ((B + 15) & ~15); }
+// TMEM columns for N <= nbox accumulator columns: a power of two, at least 32
+inline int tmem_cols_for(int nbox) {
+  int c = 32;
+  while (c < nbox) c <<= 1;
+  return c;
+}
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __global__ void __launch_bounds__(kThreads, 2)
 absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
-            const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int B, int n_h,
-            const RopeTurns turns, __nv_bfloat16* __restrict__ q_lat) {
+            const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int B, int n_h, int nbox,
+            int tcols, const RopeTurns turns, __nv_bfloat16* __restrict__ q_lat) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int h = blockIdx.x, b0 = blockIdx.y * kNB, mt = blockIdx.z;
-  const int nb = min(kNB, B - b0);
+  const int h = blockIdx.x, b0 = blockIdx.y * nbox, mt = blockIdx.z;
+  const int nb = min(nbox, B - b0);
   const int N = (nb + 15) & ~15;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [0] W M-tile, [1] q tile, [2] MMAs done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 48);
-  volatile int* ok_word = reinterpret_cast<volatile int*>(smem + OFF_BAR + 52);
+  const int off_bar = OFF_Q + 2 * nbox * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off_bar);   // [0] W M-tile, [1] q tile, [2] MMAs done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 48);
+  volatile int* ok_word = reinterpret_cast<volatile int*>(smem + off_bar + 52);
   const bool aligned = (smem_u32(smem) & 1023u) == 0;   // the 128B swizzle needs 1024-byte aligned tiles
   griddep_launch_dependents();
 
@@ -60,7 +72,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
       fence_mbar_init_cluster();
     }
     if (warp == 0) {
-      tmem_alloc(tmem_slot, 128);
+      tmem_alloc(tmem_slot, (uint32_t)tcols);
       tmem_relinquish();
     }
   }
@@ -78,7 +90,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
       mbar_arrive_expect_tx(&bars[0], kWTile);
       tma_load_3d(smem + OFF_W, &wmap, &bars[0], 0, h * kNope, 2 * mt, pol);
       griddep_wait();
-      mbar_arrive_expect_tx(&bars[1], 2 * kNB * 128);
+      mbar_arrive_expect_tx(&bars[1], 2 * nbox * 128);
       tma_load_4d(smem + OFF_Q, &qmap, &bars[1], 0, h, b0, 0, pol);
       const uint32_t idesc = idesc_f16(128, N, false, /*a_mn=*/true, /*b_mn=*/false);
       const volatile int never = 0;
@@ -91,7 +103,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
         for (int kk = 0; kk < kNope / 16; ++kk) {
           // A: 16 d rows of 128 B (64 j) per 64-j chunk, chunks 16 KB apart; B: q rows, K-major
           const uint64_t a = sdesc_sw128(wt + kk * 2048, 128 * 128, 1024);
-          const uint64_t bq = sdesc_sw128(qt + (kk >> 2) * (kNB * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bq = sdesc_sw128(qt + (kk >> 2) * (nbox * 128) + (kk & 3) * 32, 16, 1024);
           mma_ss(tmem, a, bq, idesc, kk > 0 ? 1u : 0u);
         }
       }
@@ -166,7 +178,7 @@ absorb_q_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CU
   if (!aligned) griddep_wait();
   __syncthreads();
   tc_fence_after();
-  if (aligned && warp == 0) tmem_dealloc(*tmem_slot, 128);
+  if (aligned && warp == 0) tmem_dealloc(*tmem_slot, (uint32_t)tcols);
 }
 
 }  // namespace
@@ -184,11 +196,12 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, c
                       &wmap))
       return cudaErrorInvalidValue;
   }
-  // q viewed as (64 d, head, sequence, 64-d chunk); box = one head, 128 sequences, q^C's 2 chunks
+  // q viewed as (64 d, head, sequence, 64-d chunk); box = one head, nbox sequences, q^C's 2 chunks
+  const int nbox = q_box_rows(B);
   {
     const uint64_t dims[4] = {64, (uint64_t)n_h, (uint64_t)B, 3};
     const uint64_t strides[3] = {(uint64_t)kQ * 2, (uint64_t)n_h * kQ * 2, 128};
-    const uint32_t box[4] = {64, 1, kNB, 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)nbox, 2};
     if (!encode_tiled(tmap_desc(q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
                       &qmap))
@@ -196,10 +209,12 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, const __nv_bfloat16* w_uk, c
   }
   const RopeTurns turns = rope_turns(rope);
   static std::atomic<int> attr_done[kMaxDevices];
-  const cudaError_t attr_err = smem_attr_once(absorb_q_tc, kSmem, attr_done);
+  const cudaError_t attr_err = smem_attr_once(absorb_q_tc, kSmemMax, attr_done);
   if (attr_err != cudaSuccess) return attr_err;
-  dim3 grid(n_h, ceil_div(B, kNB), kMTiles);
-  return launch_overlapped(absorb_q_tc, grid, dim3(kThreads), kSmem, st, wmap, qmap, q, pos, B, n_h, turns, q_lat);
+  dim3 grid(n_h, ceil_div(B, nbox), kMTiles);
+  const int smem = OFF_Q + 2 * nbox * 128 + kBarBytes;
+  return launch_overlapped(absorb_q_tc, grid, dim3(kThreads), smem, st, wmap, qmap, q, pos, B, n_h, nbox,
+                           tmem_cols_for(nbox), turns, q_lat);
 }
 
 }  // namespace mla
