@@ -16,8 +16,8 @@
 // 64B-swizzled [128 tokens][64 codes] chunks (the MMA's K-major operand layout).
 // O += P' · V keeps f16 operands (an 8-bit P would not keep the error budget): every
 // e4m3 code maps to the f16 of 2^-8 times its value, which is exact (see
-// e4m3x16_to_f16); the value CTA's four converter warps turn its TMA-loaded e4m3 rows
-// into 128B-swizzled f16 tiles:
+// e4m3x16_to_f16); the value CTA's eight converter warps turn its TMA-loaded e4m3 rows
+// into 128B-swizzled f16 tiles (its four row warps only rescale O and write it out):
 //   value CTA  e4m3 ring of two 32 KB steps (64 tokens x 512 columns) → two 64 KB f16
 //              stages → 8 MMAs of N = 256 per step (rows past the split are zeroed).
 // The score CTA's four extra warps only stage each tile's per-token scales. 2^-k_h
@@ -47,8 +47,11 @@ using namespace sm100;
 
 constexpr int kTile = 128;
 constexpr int kHalf = kDecodeHalf;
-constexpr int kThreads = 448;              // warp 0 TMA, 1 MMA, 2..9 row warps, 10..13 converters
-constexpr int kConvBase = 320;             // first converter thread
+constexpr int kThreads = 448;              // warp 0 TMA, 1 MMA, then per CTA role below
+constexpr int kConvBase = 320;             // score CTA: warps 2..9 softmax, 10..13 scale staging
+constexpr int kVRowWarps = 4;              // value CTA: warps 2..5 row warps (rescales, epilogue)
+constexpr int kVConvWarp = 2 + kVRowWarps; // value CTA: warps 6..13 convert codes to f16
+constexpr int kVConvWarps = kThreads / 32 - kVConvWarp;
 constexpr uint64_t kWaitNs = kDecodeWaitNs;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -216,8 +219,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       mbar_init(&bars[SB_SCLREADY + k], 128);
       mbar_init(&bars[SB_SCLFREE + k], 256);
       mbar_init(&bars[VB_E4FULL + k], 1);
-      mbar_init(&bars[VB_E4EMPTY + k], 4);
-      mbar_init(&bars[VB_F16FULL + k], 4);
+      mbar_init(&bars[VB_E4EMPTY + k], kVConvWarps);
+      mbar_init(&bars[VB_F16FULL + k], kVConvWarps);
       mbar_init(&bars[VB_F16EMPTY + k], 1);
       mbar_init(&bars[VB_PFULL + k], 1);
     }
@@ -225,7 +228,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
     mbar_init(&bars[VB_FIN], 1);
     mbar_init(&bars[VB_FLUSH], 1);
     mbar_init(&bars[VB_CREQ], 1);
-    mbar_init(&bars[VB_CDONE], 256);
+    mbar_init(&bars[VB_CDONE], 32 * kVRowWarps);
     mbar_init(&bars[VB_GO], 1);
     if (rank == 1) {
       mbar_arrive_expect_tx(&bars[VB_PFULL], kPanel + kHdr);
@@ -656,9 +659,9 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         *cmd_word = CMD_DONE;
         mbar_arrive(&bars[VB_CREQ]);
       }
-    } else if (warp >= 10) {
+    } else if (warp >= kVConvWarp) {
       // ---- converters: e4m3 step → f16 stage; rows past the split become zero ----
-      const int ct = threadIdx.x - kConvBase;
+      const int ct = threadIdx.x - 32 * kVConvWarp;
       bool ok = true;
       for (int u = 0; u < n_halves && ok; ++u) {
         const int e = u & 1, sg = u & 1;
@@ -670,10 +673,12 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         const HalfInfo hi = half_info(p, b, st, en, u, false);
         const unsigned char* vsrc = smem + V_E4 + e * kVE4;
         unsigned char* vdst = smem + V_F16 + sg * kVStage;
-        // 8 chunks x 64 rows x 64 codes: unit f = 128 k + ct is chunk f / 256, row (f % 256) / 4
+        // 8 chunks x 64 rows x 64 codes: unit f = 32 kVConvWarps k + ct is chunk f / 256,
+        // row (f % 256) / 4
+        static_assert(2048 % (32 * kVConvWarps) == 0, "units of a step split evenly over the converters");
 #pragma unroll 4
-        for (int kk = 0; kk < 16; ++kk) {
-          const int f = 128 * kk + ct, chunk = f >> 8, row = (f & 255) >> 2, c16 = f & 3;
+        for (int kk = 0; kk < 2048 / (32 * kVConvWarps); ++kk) {
+          const int f = 32 * kVConvWarps * kk + ct, chunk = f >> 8, row = (f & 255) >> 2, c16 = f & 3;
           convert_unit(vsrc + chunk * 4096 + row * 64 + 16 * c16, vdst + chunk * 8192 + row * 128, row, c16,
                        hi.load && row < hi.nvalid);
         }
@@ -687,9 +692,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       if (!ok) give_up(p, abort_flag, smem, peer);
     } else {
       // ---- row warps: rescale commands, then the epilogue ----
-      const int q = warp & 3;
+      const int q = warp & 3;   // warps 2..5: each lane quarter once, all 512 columns
       const int h = q * 32 + lane;
-      const int j = (warp - 2) >> 2;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
       int k = 0;
       bool ok = true;
@@ -708,8 +712,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
           if (__any_sync(0xffffffffu, f != 1.f)) {
             uint32_t rg[32];
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-              const uint32_t col = kOCol + 256 * j + 32 * cc;
+            for (int cc = 0; cc < 16; ++cc) {
+              const uint32_t col = kOCol + 32 * cc;
               MLA_TMEM_LD32(trow + col, rg);
               tmem_wait_ld();
 #pragma unroll
@@ -730,7 +734,7 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       const float l = fin[2 * h + 1];
       const bool good = fin_ok && *o_init_word != 0 && l > 0.f;
       const float inv = good ? 256.f / l : 0.f;   // 2^8 undoes the operand scaling
-      // Each row warp owns 32 heads x 256 columns: eight 32-column chunks, each scaled,
+      // Each row warp owns 32 heads x 512 columns: sixteen 32-column chunks, each scaled,
       // staged 128B-swizzled in a 4 KB buffer of the warp's own and written at once by a
       // TMA store that the warp issues; four buffers per warp rotate, so the stores
       // overlap the TMEM reads of the next chunks.
@@ -740,8 +744,8 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
       unsigned char* wst = smem + V_F16 + (warp - 2) * 16384;
       const int orow0 = (b * p.S + s) * p.n_h + 32 * q;
 #pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        const int chunk = 8 * j + cc;
+      for (int cc = 0; cc < 16; ++cc) {
+        const int chunk = cc;
         uint32_t r[32];
         MLA_TMEM_LD32(trow + kOCol + 32 * chunk, r);
         tmem_wait_ld();
@@ -767,11 +771,11 @@ decode_tc_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap e
         }
       }
       if (wlive && lane == 0) bulk_wait_group0();
-      if (j == 0 && h < p.n_h)
+      if (h < p.n_h)
         p.lse_part[((int64_t)b * p.S + s) * p.n_h + h] =
             good ? (m + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
       if (s == p.S_used - 1)   // slots after the last split are unused
-        for (int i = threadIdx.x - 64; i < (p.S - p.S_used) * p.n_h; i += 256)
+        for (int i = threadIdx.x - 64; i < (p.S - p.S_used) * p.n_h; i += 32 * kVRowWarps)
           p.lse_part[((int64_t)b * p.S + p.S_used) * p.n_h + i] = -INFINITY;
       tc_fence_before();
     }
