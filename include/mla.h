@@ -14,7 +14,7 @@
  *     Model - 中文验证版" (ai-papers.xuzou.cn), §"瓶颈" and §"方法适配": cache
  *     formula (d_c + d_h^R)·l, d_c = 512, d_h^R = 64, 128 heads.
  *
- * The step is four calls on the caller's stream:
+ * The step is these calls on the caller's stream (the last two, or their fused form):
  *   mla_absorb_q   q_lat[b,h] = [ W_UK[h]^T q^C[b,h]  ‖  RoPE(q^R[b,h], pos[b]) ]
  *   mla_decode_fwd split-KV attention of every head over the 576-wide cache rows
  *   mla_combine    log-sum-exp merge of the per-split partial results

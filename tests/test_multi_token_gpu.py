@@ -1,4 +1,4 @@
-"""Several new query tokens per sequence (mla_multi_token_view + the four calls) against
+"""Several new query tokens per sequence (mla_multi_token_view + the decode step) against
 the oracle's attend_multi, every element: query j of sequence b sits at L_b - T + j and
 sees only the tokens up to its own position; a query with no visible token gives 0."""
 

@@ -1,4 +1,5 @@
-"""GPU parity: the library's decode step (all four C-ABI calls) against the fp64 oracle
+"""GPU parity: the library's decode step (absorb_q, decode_fwd, combine_up_v through the
+C ABI) against the fp64 oracle
 on the same seeded inputs, within max|gpu-oracle| <= 2e-2·max|oracle| and
 sum|gpu-oracle|/sum|oracle| <= 3e-3.
 
