@@ -27,6 +27,7 @@ int main(void) {
   /* argument checks run on the host, before any CUDA call */
   if (mla_absorb_q(NULL, NULL, NULL, 1, 128, 10000.f, NULL, 0) != MLA_ERR_INVALID_ARG) return 7;
   if (mla_combine(NULL, NULL, 1, 1, 128, NULL, NULL, 0) != MLA_ERR_INVALID_ARG) return 8;
+  if (mla_combine_up_v(NULL, NULL, 1, 1, 128, NULL, NULL, NULL, NULL, 0) != MLA_ERR_INVALID_ARG) return 9;
   printf("%d %d %d\n", st, en, mla_abi_version());
   return 0;
 }
