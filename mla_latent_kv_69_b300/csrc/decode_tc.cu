@@ -148,7 +148,6 @@ template <bool kMulti>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
-                 const __grid_constant__ CUtensorMap omap,
                  float scale_log2) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = cluster_ctarank();
@@ -731,21 +730,22 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
         const int n_halves = 2 * piece_tiles(pc);
         Piece nxt;
         const bool more = next_piece(nxt);
-        // Each row warp owns 32 heads x 256 columns: eight 32-column chunks, each scaled,
-        // staged 128B-swizzled in a 4 KB buffer of the warp's own and written at once by a
-        // TMA store that the warp issues; the buffers rotate, so the stores overlap the
-        // TMEM reads. Before another piece, two buffers per warp lie in the stage of the
+        // Each row warp owns 32 heads x 256 columns: eight 32-column chunks, each scaled and
+        // staged 128B-swizzled in a 4 KB buffer of the warp's own, then read back a row
+        // per eight lanes and written with coalesced 16-byte stores (four 128-byte row
+        // pieces per instruction): the SM's TMA store path moved o_part at ~64 GB/s and
+        // paced this epilogue. Before another piece, the buffers lie in the stage of the
         // piece's last step, which the producer refills only after VB_EPIFREE; after the
-        // pair's last piece every stage is idle and each warp rotates six.
+        // pair's last piece every stage is idle.
         const int rows = p.n_h < 128 ? p.n_h : 128;
         const int wrows = rows < 32 ? rows : 32;
         const bool wlive = 32 * q < rows;
-        const int nbuf = more ? 2 : 6;
         unsigned char* wst = more ? smem + V_CST + (int)((u_base + n_halves - 1) % kCStages) * kCStage +
                                         (warp - 2) * 2 * kEpiBuf
                                   : smem + V_CST + (warp - 2) * 6 * kEpiBuf;
         const int64_t orow0 = part_row(p, pc.b, pc.slot) + 32 * q;
         uint32_t r[32];
+        const int ux = lane & 7, usub = lane >> 3;   // read-back: 16-byte unit, row within four
 #pragma unroll 1
         for (int cc = 0; cc < 8; ++cc) {
           const int chunk = 8 * j + cc;
@@ -756,14 +756,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
             mbar_arrive(&bars[VB_CDONE]);
           }
           if (!wlive) continue;
-          unsigned char* buf = wst + (cc % nbuf) * kEpiBuf;
-          if (cc >= nbuf) {   // this buffer's previous store has to have read it
-            if (lane == 0) {
-              if (more) bulk_wait_group_read<1>();
-              else bulk_wait_group_read<5>();
-            }
-            __syncwarp();
-          }
+          unsigned char* buf = wst + (cc & 1) * kEpiBuf;
           if (lane < wrows) {
             unsigned char* dst = buf + lane * 128;
 #pragma unroll
@@ -772,14 +765,17 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap smap,
                   make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
                               __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&omap, buf, 0, (int)orow0, chunk);
-            bulk_commit_group();
+          // rows 4 k + usub: head 32 q + row of o_part, columns 32 chunk + 4 ux .. + 3
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int row = 4 * k + usub;
+            if (row < wrows) {
+              const float4 v = *reinterpret_cast<const float4*>(buf + row * 128 + ((ux ^ (row & 7)) << 4));
+              *reinterpret_cast<float4*>(p.o_part + (orow0 + row) * kLatent + 32 * chunk + 4 * ux) = v;
+            }
           }
         }
-        if (wlive && lane == 0) bulk_wait_group_read0();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[VB_EPIFREE]);   // this warp's staging is free again
         if (j == 0 && h < p.n_h)
@@ -814,17 +810,6 @@ bool make_row_map(const void* base, int64_t rows, int box_rows, int box_chunks, 
                       map);
 }
 
-// 3D map over the fp32 partial results [rows][512] seen as (32 values, row, 16 chunks of
-// 32), 128B swizzle; a box is `box_rows` rows (32, or n_h when smaller) x one chunk.
-bool make_out_map(float* base, int64_t rows, int box_rows, CUtensorMap* map) {
-  const uint64_t dims[3] = {32, (uint64_t)rows, (uint64_t)(kLatent / 32)};
-  const uint64_t strides[2] = {(uint64_t)kLatent * 4, 128};
-  const uint32_t box[3] = {32, (uint32_t)box_rows, 1};
-  return encode_tiled(tmap_desc(base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE),
-                      map);
-}
-
 }  // namespace
 
 bool decode_tc_supported(const DecodeParams& p) {
@@ -836,12 +821,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   (void)max_seq_len;
   // score side: 128 rows x 3 chunks (contiguous) or, for paged caches, 64 rows x 1 chunk
   // through the value map; value side: 64 rows x 8 chunks; queries: n_h rows x 3 chunks
-  // (partial-result store: n_h rows x 8 chunks of 32 fp32)
-  CUtensorMap smap, vmap, qmap, omap;
+  CUtensorMap smap, vmap, qmap;
   if (!make_row_map(p.data, p.num_rows, p.block_table ? 64 : kTile, p.block_table ? 1 : 3, &smap) ||
       !make_row_map(p.data, p.num_rows, 64, 8, &vmap) ||
-      !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap) ||
-      !make_out_map(p.o_part, (int64_t)p.B * p.S * p.n_h, p.n_h < 32 ? p.n_h : 32, &omap))
+      !make_row_map(p.q_lat, (int64_t)p.B * p.n_h, p.n_h < 128 ? p.n_h : 128, 3, &qmap))
     return cudaErrorInvalidValue;
   static std::atomic<int> attr_multi[kMaxDevices], attr_single[kMaxDevices];
   const cudaError_t attr_err = p.balanced ? smem_attr_once(decode_tc_kernel<true>, kSmemBytes, attr_multi)
@@ -850,9 +833,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int max_seq_len, cudaStream_
   const float scale_log2 = p.scale * 1.4426950408889634f;
   if (p.balanced)
     return launch_overlapped(decode_tc_kernel<true>, dim3((unsigned)(2 * p.pairs)), dim3(kThreads), kSmemBytes, st, p,
-                             smap, vmap, qmap, omap, scale_log2);
+                             smap, vmap, qmap, scale_log2);
   return launch_overlapped(decode_tc_kernel<false>, dim3((unsigned)(2 * (int64_t)p.B * p.S_used)), dim3(kThreads),
-                           kSmemBytes, st, p, smap, vmap, qmap, omap, scale_log2);
+                           kSmemBytes, st, p, smap, vmap, qmap, scale_log2);
 }
 
 int decode_tc_num_splits(int B, int tiles, int n_h, int sms) {
