@@ -32,6 +32,9 @@ Modules:
   results, and the cache-size arithmetic.
 * ``fp8_e4m3`` — the e4m3 ("fn": finite, no infinities) codec written from the
   format definition, and the per-token amax/448 row quantiser.
+* ``fp6_e2m3`` — the e2m3 (6-bit) codec, the per-64-element-group quantiser and the
+  four-codes-in-three-bytes packing of the ~6-bit cache reading; no CUDA path uses it
+  yet.
 """
 
-from . import fp8_e4m3, mla_oracle  # noqa: F401
+from . import fp6_e2m3, fp8_e4m3, mla_oracle  # noqa: F401

@@ -2,8 +2,8 @@
 
 Each case rewrites one line of one oracle function (a flipped sign, a swapped operand,
 a wrong constant or index), installs the rewritten function in place of the original
-for the duration of the case, runs the pin tests of test_oracle.py / test_fp8_codec.py
-against it, and requires that at least one pin fails. The mistakes are planted only in
+for the duration of the case, runs the pin tests of test_oracle.py / test_fp8_codec.py /
+test_fp6_codec.py against it, and requires that at least one pin fails. The mistakes are planted only in
 this process, on the CPU; the oracle's files are not touched.
 """
 
@@ -13,8 +13,10 @@ import textwrap
 import numpy as np
 import pytest
 
+import test_fp6_codec as P6
 import test_fp8_codec as PF
 import test_oracle as PO
+from oracle import fp6_e2m3 as F6
 from oracle import fp8_e4m3 as F
 from oracle import mla_oracle as M
 
@@ -133,3 +135,37 @@ def test_fp8_pins_catch_planted_mistake(monkeypatch, fname, old, new):
         monkeypatch.setattr(F, "DECODE_TABLE", np.array([mutant(c) for c in range(256)], dtype=np.float64))
         monkeypatch.setattr(F, "_POS", F.DECODE_TABLE[:0x7F].copy())
     assert _failing_pins(PF, _fp8_param_pins()), f"no pin notices {fname}: {old!r} -> {new!r}"
+
+
+
+def _fp6_param_pins():
+    """The parametrised code-value pin, run over its own parameter list."""
+    cases = next(m.args[1] for m in P6.test_code_value_definition.pytestmark if m.name == "parametrize")
+
+    def listed_codes():
+        for code, value in cases:
+            P6.test_code_value_definition(code, value)
+    return [("test_code_value_definition[listed]", listed_codes)]
+
+
+FP6_MUTANTS = [
+    ("code_value", "v = (1.0 + m / 8.0) * 2.0 ** (e - 1)", "v = (1.0 + m / 8.0) * 2.0 ** (e - 2)"),
+    ("code_value", "v = m * 2.0 ** -3", "v = m * 2.0 ** -4"),
+    ("code_value", "m = code & 0x7", "m = (code >> 1) & 0x7"),
+    ("encode", "take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))", "take_hi = d_hi <= d_lo"),
+    ("encode", "(np.signbit(x).astype(np.int64) << 5)", "(np.signbit(x).astype(np.int64) << 4)"),
+    ("quantize_groups", "amax / np.float32(E2M3_MAX)", "amax / np.float32(6.0)"),
+    ("pack", "(c[..., 2] << 12)", "(c[..., 2] << 11)"),
+    ("unpack", "(w >> (6 * k)) & 0x3F", "(w >> (6 * k)) & 0x1F"),
+]
+
+
+@pytest.mark.parametrize("fname,old,new", FP6_MUTANTS, ids=[f"{m[0]}:{m[2][:28]}" for m in FP6_MUTANTS])
+def test_fp6_pins_catch_planted_mistake(monkeypatch, fname, old, new):
+    assert not _failing_pins(P6, _fp6_param_pins())
+    mutant = _mutant(getattr(F6, fname), old, new)
+    monkeypatch.setattr(F6, fname, mutant)
+    if fname == "code_value":   # the decode table is built from code_value at import
+        monkeypatch.setattr(F6, "DECODE_TABLE", np.array([mutant(c) for c in range(64)], dtype=np.float64))
+        monkeypatch.setattr(F6, "_POS", F6.DECODE_TABLE[:0x20].copy())
+    assert _failing_pins(P6, _fp6_param_pins()), f"no pin notices {fname}: {old!r} -> {new!r}"
