@@ -399,6 +399,27 @@ def quantize_fp8(rows, codes=None, scales=None, stream=None):
     return codes, scales
 
 
+def quantize_fp6(rows, packed=None, scales=None, stream=None):
+    """rows [..., 576] bf16 → (packed uint8 [..., 432], scales fp32 [..., 9]): the ~6-bit
+    cache format of include/mla.h, mla_quantize_fp6 (e2m3 codes in 64-element groups)."""
+    if rows.dtype != torch.bfloat16 or rows.shape[-1] != D_ROW:
+        raise TypeError("rows must be bf16 [..., 576]")
+    lead = tuple(rows.shape[:-1])
+    n = int(math.prod(lead))
+    if packed is None:
+        packed = torch.empty(*lead, D_ROW * 6 // 8, dtype=torch.uint8, device=rows.device)
+    if scales is None:
+        scales = torch.empty(*lead, D_ROW // 64, dtype=torch.float32, device=rows.device)
+    _need(rows, "rows", torch.bfloat16)
+    _need(packed, "packed", torch.uint8, (*lead, D_ROW * 6 // 8))
+    _need(scales, "scales", torch.float32, (*lead, D_ROW // 64))
+    if n == 0:   # empty tensors may have no storage to point at
+        return packed, scales
+    dev = _one_device(rows=rows, packed=packed, scales=scales)
+    _call("mla_quantize_fp6", dev, _ptr(rows), n, _ptr(packed), _ptr(scales), stream=stream)
+    return packed, scales
+
+
 def decode_step(q, w_uk, w_uv, cache: Cache, seq_lens, pos, max_seq_len: int, n_splits: int = 0,
                 softmax_scale: float | None = None, rope_base: float = 10000.0, bufs: dict | None = None,
                 status=None, stream=None, yarn: Yarn | None = None, latent: bool = True):

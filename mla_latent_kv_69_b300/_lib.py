@@ -27,7 +27,7 @@ EXPORTS = [
     "mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
     "mla_num_splits", "mla_split_range", "mla_status_string", "mla_abi_version", "mla_decode_kernel",
     "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append", "mla_absorb_q_ex",
-    "mla_cache_append_ex", "mla_multi_token_view", "mla_combine_up_v",
+    "mla_cache_append_ex", "mla_multi_token_view", "mla_combine_up_v", "mla_quantize_fp6",
 ]
 
 
@@ -85,6 +85,7 @@ def _load():
     lib.mla_multi_token_view.argtypes = [ctypes.POINTER(MlaCache), vp, i32, i32, i32, vp, vp, vp, i32,
                                          ctypes.POINTER(MlaCache), vp]
     lib.mla_quantize_fp8.argtypes = [vp, i64, vp, vp, vp]
+    lib.mla_quantize_fp6.argtypes = [vp, i64, vp, vp, vp]
     lib.mla_num_splits.argtypes = [i32, i32, i32]
     lib.mla_decode_kernel.argtypes = [i32, i32]
     lib.mla_split_range.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
@@ -93,7 +94,7 @@ def _load():
     for fn in ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_up_v", "mla_quantize_fp8",
                "mla_num_splits", "mla_split_range", "mla_abi_version", "mla_decode_kernel",
                "mla_decode_combine_static", "mla_test_decode_stalled", "mla_cache_append", "mla_absorb_q_ex",
-               "mla_cache_append_ex", "mla_multi_token_view", "mla_combine_up_v"):
+               "mla_cache_append_ex", "mla_multi_token_view", "mla_combine_up_v", "mla_quantize_fp6"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
