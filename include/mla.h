@@ -294,18 +294,20 @@ MLA_API mla_status mla_quantize_fp8(const void* rows, int64_t num_rows, uint8_t*
  * mla_quantize_fp6 — bf16 rows → the ~6-bit cache format (a reading of the pages'
  *   "about 6 bits per element": "DeepSeek-V2 机制拆解", §"推理参数与 128K 上下文的使用注意";
  *   "中文验证版", §"瓶颈"; the pages give no format). No decode kernel reads it yet.
- *   Each row's 576 elements form nine groups of 64; group g has
- *   scale_g = amax_g / 7.5 (1 for an all-zero group) and codes e2m3(x / scale_g):
- *   6 bits s ee mmm, exponent bias 1, values up to 7.5, fp32 division, round to
- *   nearest with ties to the even code, saturating. Codes 4t .. 4t+3 of a row are the
- *   little-endian 24-bit word c0 | c1 << 6 | c2 << 12 | c3 << 18 at bytes 3t .. 3t+2.
+ *   The layout is the published microscaling one for 6-bit elements (MXFP6 E2M3):
+ *   each row's 576 elements form eighteen blocks of 32 that share a power-of-two
+ *   scale X = 2^se, se = floor(log2 amax) - 2 clamped to -127..127 (0 for an all-zero
+ *   block), stored as the byte se + 127; each element is coded e2m3(x / X): 6 bits
+ *   s ee mmm, exponent bias 1, values up to 7.5, round to nearest with ties to the
+ *   even code, saturating. Codes 4t .. 4t+3 of a row are the little-endian 24-bit word
+ *   c0 | c1 << 6 | c2 << 12 | c3 << 18 at bytes 3t .. 3t+2.
  *   rows [num_rows, 576] bf16 (finite values; 16-byte aligned);
- *   packed [num_rows, 432] uint8 out; scales [num_rows, 9] fp32 out (4-byte aligned).
- *   Errors: NULL pointers, misalignment, num_rows < 0 -> MLA_ERR_INVALID_ARG;
+ *   packed [num_rows, 432] uint8 out; scales [num_rows, 18] uint8 out.
+ *   Errors: NULL pointers, misaligned rows, num_rows < 0 -> MLA_ERR_INVALID_ARG;
  *   num_rows = 0 is a no-op.
  */
 MLA_API mla_status mla_quantize_fp6(const void* rows, int64_t num_rows, uint8_t* packed,
-                            float* scales, cudaStream_t stream);
+                            uint8_t* scales, cudaStream_t stream);
 
 /*
  * mla_decode_combine_static — mla_decode_fwd followed by mla_combine with the split

@@ -400,8 +400,9 @@ def quantize_fp8(rows, codes=None, scales=None, stream=None):
 
 
 def quantize_fp6(rows, packed=None, scales=None, stream=None):
-    """rows [..., 576] bf16 → (packed uint8 [..., 432], scales fp32 [..., 9]): the ~6-bit
-    cache format of include/mla.h, mla_quantize_fp6 (e2m3 codes in 64-element groups)."""
+    """rows [..., 576] bf16 → (packed uint8 [..., 432], scale bytes uint8 [..., 18]): the
+    ~6-bit cache format of include/mla.h, mla_quantize_fp6 (e2m3 codes in 32-element
+    blocks sharing a power-of-two scale)."""
     if rows.dtype != torch.bfloat16 or rows.shape[-1] != D_ROW:
         raise TypeError("rows must be bf16 [..., 576]")
     lead = tuple(rows.shape[:-1])
@@ -409,10 +410,10 @@ def quantize_fp6(rows, packed=None, scales=None, stream=None):
     if packed is None:
         packed = torch.empty(*lead, D_ROW * 6 // 8, dtype=torch.uint8, device=rows.device)
     if scales is None:
-        scales = torch.empty(*lead, D_ROW // 64, dtype=torch.float32, device=rows.device)
+        scales = torch.empty(*lead, D_ROW // 32, dtype=torch.uint8, device=rows.device)
     _need(rows, "rows", torch.bfloat16)
     _need(packed, "packed", torch.uint8, (*lead, D_ROW * 6 // 8))
-    _need(scales, "scales", torch.float32, (*lead, D_ROW // 64))
+    _need(scales, "scales", torch.uint8, (*lead, D_ROW // 32))
     if n == 0:   # empty tensors may have no storage to point at
         return packed, scales
     dev = _one_device(rows=rows, packed=packed, scales=scales)

@@ -1,5 +1,5 @@
-"""e2m3 (6-bit float) codec, its per-group quantiser and the 3-byte packing of the
-~6-bit cache reading, from the format definition.
+"""e2m3 (6-bit float) codec, its block quantiser and the 3-byte packing of the ~6-bit
+cache reading, from the format definitions.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring): the library never imports this.
 
@@ -14,16 +14,22 @@ Format (6 bits, s ee mmm, exponent bias 1, no infinities and no NaN):
 The largest magnitude is 1.875 · 2^2 = 7.5; the positive values are k/8 for k = 0..15,
 k/4 for k = 8..15 and k/2 for k = 8..15.
 
-Grouping: each cached token's 576 elements form nine groups of 64 consecutive
-elements; group g has one fp32 scale = amax_g / 7.5 (an all-zero group gets 1), and
-code = encode(x / scale) with the division in fp32. Encoding rounds to the nearest
-value, ties to the even code (even mantissa), and saturates at ±7.5; inputs are
-finite (cache rows are bf16 values).
+Blocks (the published microscaling layout for 6-bit elements, MXFP6 E2M3): each cached
+token's 576 elements form eighteen blocks of 32 consecutive elements; block b shares
+one power-of-two scale X_b = 2^(floor(log2 amax_b) - 2), the 2 being the exponent of
+e2m3's largest value (7.5 = 1.875 · 2^2), stored as the 8-bit biased exponent
+(E8M0: byte = exponent + 127, clamped to 0..254); an all-zero block gets X = 1. Each
+element's code is encode(x / X); x / X is exact (a power of two) and lies in [0, 8), so
+only elements above 7.5 · X saturate. Power-of-two block scales are what the tensor
+cores' block-scaled 8/6/4-bit MMA applies inside the K reduction; a per-token scale
+(the e4m3 stand-in) can be pulled out of QK^T, a per-block one cannot. Encoding rounds
+to the nearest value, ties to the even code (even mantissa), and saturates at ±7.5;
+inputs are finite (cache rows are bf16 values).
 
 Packing: four consecutive codes c0..c3 of a token form the 24-bit little-endian word
 c0 | c1 << 6 | c2 << 12 | c3 << 18, stored as its three bytes in order; a token is 432
-bytes of codes plus nine fp32 scales (36 bytes), 468 bytes in all against 580 for the
-e4m3 codes with one scale per token.
+bytes of codes plus eighteen scale bytes, 450 bytes in all against 580 for the e4m3
+codes with one fp32 scale per token.
 """
 
 from __future__ import annotations
@@ -31,8 +37,10 @@ from __future__ import annotations
 import numpy as np
 
 E2M3_MAX = 7.5
-GROUP = 64
+E2M3_EMAX = 2          # exponent of the largest e2m3 value
+BLOCK = 32
 CODE_BITS = 6
+SCALE_BIAS = 127
 
 
 def code_value(code: int) -> float:
@@ -72,28 +80,37 @@ def encode(x) -> np.ndarray:
     return (mag | (np.signbit(x).astype(np.int64) << 5)).astype(np.uint8)
 
 
-def quantize_groups(x):
-    """x [T, D] (fp32 values, D a multiple of 64) → (codes uint8 [T, D], scales fp32 [T, D/64]).
+def block_exponents(x) -> np.ndarray:
+    """x [T, D] fp32 → the shared exponent of each 32-element block, floor(log2 amax) - 2,
+    clamped to -127..127 (0 for an all-zero block), as int64 [T, D/32]."""
+    x = np.asarray(x, dtype=np.float32)
+    T, D = x.shape
+    if D % BLOCK:
+        raise ValueError("the row length must be a multiple of 32")
+    amax = np.max(np.abs(x.reshape(T, D // BLOCK, BLOCK)), axis=-1).astype(np.float64)
+    _, e = np.frexp(amax)                   # amax = f · 2^e with f in [0.5, 1): floor(log2 amax) = e - 1
+    se = np.clip(e.astype(np.int64) - 1 - E2M3_EMAX, -SCALE_BIAS, SCALE_BIAS)
+    return np.where(amax > 0, se, 0)
 
-    scale_g = amax_g / 7.5 in fp32 over each 64-element group (an all-zero group gets 1),
-    code    = encode(x / scale_g) with the division in fp32.
+
+def quantize_blocks(x):
+    """x [T, D] (fp32 values, D a multiple of 32) → (codes uint8 [T, D], scale bytes uint8 [T, D/32]).
+
+    code = encode(x · 2^-se) for the block's shared exponent se; scale byte = se + 127.
     """
     x = np.asarray(x, dtype=np.float32)
     T, D = x.shape
-    if D % GROUP:
-        raise ValueError("the row length must be a multiple of 64")
-    g = x.reshape(T, D // GROUP, GROUP)
-    amax = np.max(np.abs(g), axis=-1).astype(np.float32)
-    scale = np.where(amax > 0, amax / np.float32(E2M3_MAX), np.float32(1.0)).astype(np.float32)
-    y = (g / scale[..., None]).astype(np.float32)
-    return encode(y).reshape(T, D), scale
+    se = block_exponents(x)
+    y = np.ldexp(x.reshape(T, D // BLOCK, BLOCK), (-se)[..., None].astype(np.int32)).astype(np.float32)
+    return encode(y).reshape(T, D), (se + SCALE_BIAS).astype(np.uint8)
 
 
-def dequantize_groups(codes, scales) -> np.ndarray:
-    """Inverse of quantize_groups in fp64: value = decode(code) · scale of its group."""
+def dequantize_blocks(codes, scale_bytes) -> np.ndarray:
+    """Inverse of quantize_blocks in fp64: value = decode(code) · 2^(byte - 127) of its block."""
     codes = np.asarray(codes, dtype=np.uint8)
     T, D = codes.shape
-    v = decode(codes).reshape(T, D // GROUP, GROUP) * np.asarray(scales, dtype=np.float64)[..., None]
+    x = 2.0 ** (np.asarray(scale_bytes, dtype=np.float64) - SCALE_BIAS)
+    v = decode(codes).reshape(T, D // BLOCK, BLOCK) * x[..., None]
     return v.reshape(T, D)
 
 
@@ -120,5 +137,5 @@ def unpack(packed) -> np.ndarray:
 
 
 def bytes_per_token(d: int = 576) -> int:
-    """Packed codes plus the group scales of one cached token of d elements."""
-    return d * CODE_BITS // 8 + (d // GROUP) * 4
+    """Packed codes plus the block scale bytes of one cached token of d elements."""
+    return d * CODE_BITS // 8 + d // BLOCK

@@ -1,8 +1,9 @@
-"""Pins of the e2m3 codec, group quantiser and 3-byte packing (oracle/fp6_e2m3.py)
+"""Pins of the e2m3 codec, block quantiser and 3-byte packing (oracle/fp6_e2m3.py)
 against the format's definition, stated here independently of the oracle's code:
 the positive e2m3 values are three grids (k/8 below 2, k/4 from 2 to 4, k/2 from 4 to
 7.5), the sign bit negates, encoding is nearest-with-ties-to-even by brute force over
-that grid, and the packing is a little-endian 24-bit word per four codes."""
+that grid, a block's shared exponent is floor(log2 amax) - 2 (math.frexp), and the
+packing is a little-endian 24-bit word per four codes."""
 
 import numpy as np
 import pytest
@@ -65,29 +66,34 @@ def test_saturates_and_rejects_non_finite():
         F.encode(np.array([np.nan], np.float32))
 
 
-def test_quantize_groups_properties():
+def test_quantize_blocks_properties():
+    import math
     rng = np.random.default_rng(7)
-    x = (rng.standard_normal((5, 576)) * rng.choice([1e-3, 1.0, 30.0], size=(5, 9)).repeat(64, axis=1))
-    x[2, 64:128] = 0.0                                 # an all-zero group
+    x = (rng.standard_normal((5, 576)) * rng.choice([1e-30, 1e-3, 1.0, 30.0, 1e30], size=(5, 18)).repeat(32, axis=1))
+    x[2, 64:96] = 0.0                                  # an all-zero block
     x = x.astype(np.float32)
-    codes, scales = F.quantize_groups(x)
-    assert codes.shape == (5, 576) and scales.shape == (5, 9) and scales.dtype == np.float32
-    g = x.reshape(5, 9, 64)
-    amax = np.abs(g).max(axis=-1)
-    np.testing.assert_array_equal(scales, np.where(amax > 0, amax / np.float32(7.5), 1).astype(np.float32))
-    assert np.all(codes[2, 64:128] == 0)
-    # each non-zero group's largest element lands on +-7.5
-    c = codes.reshape(5, 9, 64)
-    idx = np.abs(g).argmax(axis=-1)
-    top = np.take_along_axis(c, idx[..., None], axis=-1)[..., 0]
-    live = amax > 0
-    assert np.all((top[live] & 0x1F) == 0x1F)
-    # error within half a grid step of the element's binade (0.0625 below 2, 0.125 below
-    # 4, 0.25 above), in units of the group's scale, plus fp32 rounding of x / scale
-    back = F.dequantize_groups(codes, scales).reshape(5, 9, 64)
-    y = np.abs(g / scales[..., None])
+    codes, sbytes = F.quantize_blocks(x)
+    assert codes.shape == (5, 576) and sbytes.shape == (5, 18) and sbytes.dtype == np.uint8
+    g = x.reshape(5, 18, 32).astype(np.float64)
+    for t in range(5):
+        for b in range(18):
+            amax = float(np.abs(g[t, b]).max())
+            if amax == 0:
+                assert sbytes[t, b] == 127 and np.all(codes[t, 32 * b:32 * b + 32] & 0x1F == 0)
+                continue
+            m, e = math.frexp(amax)                    # amax = m 2^e, m in [0.5, 1)
+            se = e - 1 - 2
+            assert sbytes[t, b] == se + 127
+            assert 4.0 <= amax / 2.0 ** se < 8.0
+    # every element within half a grid step of its binade, or saturated at 7.5 X
+    X = 2.0 ** (sbytes.astype(np.float64) - 127)[..., None]
+    back = F.dequantize_blocks(codes, sbytes).reshape(5, 18, 32)
+    y = np.abs(g / X)
     half = np.where(y < 2, 1 / 16, np.where(y < 4, 1 / 8, 1 / 4))
-    assert np.all(np.abs(back - g) <= (half * (1 + 1e-6) + 1e-7) * scales[..., None])
+    err = np.abs(back - g) / X
+    sat = y > 7.5
+    assert np.all(err[~sat] <= half[~sat])
+    assert np.all(np.abs(err[sat] - (y[sat] - 7.5)) <= 1e-12)
 
 
 def test_pack_bit_layout():
@@ -107,7 +113,7 @@ def test_pack_roundtrip_and_sizes():
 
 
 def test_bytes_per_token_and_the_pages_6bit_arithmetic():
-    assert F.bytes_per_token() == 432 + 36
+    assert F.bytes_per_token() == 432 + 18
     # [B] §瓶颈: 128K tokens x 60 layers of (512 + 64) elements at 6 bits is about 3.4 GB
     codes_only = 131072 * 60 * 576 * 6 / 8
     assert abs(codes_only / 1e9 - 3.4) < 0.01

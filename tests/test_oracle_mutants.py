@@ -154,7 +154,8 @@ FP6_MUTANTS = [
     ("code_value", "m = code & 0x7", "m = (code >> 1) & 0x7"),
     ("encode", "take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))", "take_hi = d_hi <= d_lo"),
     ("encode", "(np.signbit(x).astype(np.int64) << 5)", "(np.signbit(x).astype(np.int64) << 4)"),
-    ("quantize_groups", "amax / np.float32(E2M3_MAX)", "amax / np.float32(6.0)"),
+    ("block_exponents", "e.astype(np.int64) - 1 - E2M3_EMAX", "e.astype(np.int64) - E2M3_EMAX"),
+    ("quantize_blocks", "(-se)[..., None]", "(1 - se)[..., None]"),
     ("pack", "(c[..., 2] << 12)", "(c[..., 2] << 11)"),
     ("unpack", "(w >> (6 * k)) & 0x3F", "(w >> (6 * k)) & 0x1F"),
 ]
