@@ -40,6 +40,28 @@ int sm_count() {
   return cached[dev];
 }
 
+// Uniform split count of the e4m3 decode (one SM pair per (sequence, split)). Its
+// 128-token tile takes ~3.6 us on the score CTA's 8-bit MMAs and a unit ~15 us to start
+// and drain (timestamps of the kernel at B = 128 x 8192), and every split adds an n_h x
+// 2 KB partial that the merge reads back (~0.13 us per (sequence, split) at 128 heads
+// over the GPU); the count minimises waves x unit time plus those reads.
+int e4m3_num_splits(int B, int max_seq_len, int n_h, int pairs) {
+  const int t = (max_seq_len + 127) / 128;
+  if (t <= 1 || pairs < 1) return 1;
+  int best = 1;
+  double best_us = 1e30;
+  for (int S = 1; S <= t && S <= MLA_MAX_SPLITS; ++S) {
+    const int per = (t + S - 1) / S;
+    const int waves = (B * S + pairs - 1) / pairs;
+    const double us = waves * (per * 3.6 + 15.0) + 0.13 * (double)B * S * n_h / 128.0;
+    if (us < best_us - 1e-9) {
+      best_us = us;
+      best = S;
+    }
+  }
+  return best;
+}
+
 // A validated mla_rope: base > 1; plain (yarn_scale = 1) or YaRN with scale > 1,
 // 0 <= alpha < beta and original_max_pos >= 1.
 bool rope_spec(const mla_rope* r, RopeSpec* out) {
@@ -183,7 +205,9 @@ mla_status decode_fwd_impl(const void* q_lat, const mla_cache* cache, const int3
       // contiguous caches and e4m3: one pair per (sequence, split), uniform splits sized
       // for the longest sequence, within the slots
       const int tiles = ceil_div(max_seq_len, kPage);
-      const int su = tiles <= 1 ? 1 : decode_tc_num_splits(B, tiles, n_h, sm_count());
+      const int su = tiles <= 1                          ? 1
+                     : cache->dtype == MLA_KV_FP8_E4M3 ? e4m3_num_splits(B, max_seq_len, n_h, sm_count() / 2)
+                                                       : decode_tc_num_splits(B, tiles, n_h, sm_count());
       p.S_used = su < S ? su : S;
     }
   }
